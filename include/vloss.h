@@ -1,0 +1,181 @@
+/*
+ * libvloss: fused per-token losses over rows of vocabulary logits (GB300, sm_103a).
+ *
+ * One row of fp32 logits s (length V) per token.  Each row gets one
+ * max / log-sum-exp reduction, m = max_j s_j, lnS = ln sum_j exp(s_j - m),
+ * lse = m + lnS, from which the entry points below produce:
+ *
+ *   cross-entropy   loss = lse - s[label],  gradient scale * (softmax(s) - onehot(label))
+ *                   (aprender-train 0.36.0, entrenar/autograd/wgpu_cross_entropy.rs:
+ *                    module doc, forward_async, read_loss, backward);
+ *   top-k KL        loss = sum_q p_q (ln p_q - (s[id_q] - lse)),
+ *                   gradient coef * (softmax(s) - p_T), p_T the teacher's top-k
+ *                   probabilities scattered onto their ids
+ *                   (cortiq-engine 0.8.21, src/gpu_wgpu/train_head.rs: module doc, kl_rows);
+ *   teacher top-k   the k largest logits, descending, ties to the lower id, with
+ *                   probabilities renormalised over the k (train_head.rs: topk_rows);
+ *   acc_add         a += b, the sum of per-slice partials (train_head.rs: acc_add, head_kl).
+ *
+ * Conventions shared by every entry point:
+ *
+ *  - Pointers are DEVICE pointers owned by the caller, except where a comment says
+ *    otherwise.  The library allocates no memory and keeps no pointer after return.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  They never synchronise and never read results back; argument errors
+ *    are detected on the host and returned before anything is launched.
+ *  - Logits are row-major fp32: row t starts at logits + t * ld; `ld >= V` is the
+ *    row stride in elements.  Any alignment of `logits` and any `ld` is accepted
+ *    (the kernels stream the 16-byte-aligned body of each row with bulk copies and
+ *    handle up to 3 leading and 3 trailing elements with plain loads).
+ *  - A vocabulary slice is the column range [col0, col0 + ncols) of every row;
+ *    in-place entry points write exactly that range of rows [0, ntok) and nothing else.
+ *  - The loss window [loss_start, loss_end), 0 <= loss_start <= loss_end <= ntok,
+ *    selects the tokens that count (CEForwardParams / CEBackwardParams of the
+ *    cross-entropy page).  Rows outside it get loss 0 and an all-zero gradient.
+ *  - Labels and teacher ids are uint32.  A label or id >= V is a data error: it is
+ *    counted into *err (when err is not NULL) with atomicAdd, its term is left out,
+ *    and a CE loss with a bad label is NaN.  No kernel traps.
+ *  - Row statistics `stats` are pairs (m, lnS) per row, [ntok][2] fp32.  They carry the
+ *    log-sum-exp of a row between calls more precisely than lse itself: m is exact and
+ *    lnS is small exactly when the row is peaked, so the softmax of a later sliced pass
+ *    keeps full fp32 accuracy.  Passing only lse costs up to half an ulp of lse in the
+ *    exponent of every softmax value.
+ *  - A wait inside a kernel that exceeds about two seconds (a bug, never a normal
+ *    condition) ends that kernel early with its outputs incomplete and sets a flag
+ *    that vl_watchdog_flag() reports.
+ */
+#ifndef VLOSS_H
+#define VLOSS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VL_API __attribute__((visibility("default")))
+#else
+#define VL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vl_status {
+    VL_OK = 0,
+    VL_EINVAL = 1,        /* bad argument: NULL where required, size or window out of range */
+    VL_ELAUNCH = 2,       /* a CUDA call failed; vl_last_error_string() says which */
+    VL_EUNSUPPORTED = 3   /* valid request beyond this build's limits (e.g. k > VL_KL_KMAX) */
+} vl_status;
+
+/* Limits of this build. */
+#define VL_KL_KMAX 1024      /* teacher support per row for vl_kl_topk_inplace */
+#define VL_TOPK_KMAX 2048    /* k of vl_topk_rows (the page's bound for topk_rows) */
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+VL_API int vl_version(void);
+
+/* Static text for a status code. */
+VL_API const char* vl_status_string(vl_status s);
+
+/* Text of the last error raised on the calling host thread ("" if none). */
+VL_API const char* vl_last_error_string(void);
+
+/*
+ * Cross-entropy forward (wgpu_cross_entropy.rs: module doc "loss = -logits[label] +
+ * logsumexp(logits)", forward_async, read_loss).  Reads logits rows [0, ntok), columns
+ * [0, V); writes for every row lse[t] (and stats[t] when not NULL), and loss[t] =
+ * lse[t] - s_t[label_t] inside the window, 0 outside.  mean (nullable, one float) gets
+ * sum of loss over the window / (loss_end - loss_start), 0 for an empty window, as
+ * read_loss computes it.
+ *   logits [ntok][ld] fp32 (read only)   labels [ntok] u32   loss [ntok] fp32
+ *   lse [ntok] fp32 (nullable)           stats [ntok][2] fp32 (nullable)
+ *   mean: one fp32 (nullable)            err: one int32 counter (nullable)
+ */
+VL_API vl_status vl_ce_fwd(const float* logits, int64_t ld, int64_t ntok, int64_t V,
+                    const uint32_t* labels, int64_t loss_start, int64_t loss_end,
+                    float* loss, float* lse, float* stats, float* mean,
+                    int32_t* err, void* stream);
+
+/*
+ * Cross-entropy backward in place over a vocabulary slice (wgpu_cross_entropy.rs:
+ * backward, "logits[i] = (softmax(logits)[i] - one_hot(label)[i]) * scale").  For rows in
+ * the window, columns j in [col0, col0 + ncols):
+ *     logits[t][j] = scale * (exp(s_t,j - lse_t) - [j == label_t]),
+ * rows outside the window are zeroed.  The page fixes scale = 1 / max(1, window); here it
+ * is the caller's argument.  The row statistics come from `stats` when not NULL, else from
+ * `lse` (one of them is required).  loss_part (nullable) gets, per row, the slice's share
+ * of the CE loss: lse - s[label] when the label lies in the slice and the row is in the
+ * window, else 0.
+ */
+VL_API vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
+                            int64_t col0, int64_t ncols, const uint32_t* labels,
+                            const float* lse, const float* stats,
+                            int64_t loss_start, int64_t loss_end, float scale,
+                            float* loss_part, int32_t* err, void* stream);
+
+/*
+ * Cross-entropy forward and backward in one pass over each row: the row is read from
+ * HBM once and the gradient written once.  Outputs as vl_ce_fwd, then logits rows are
+ * overwritten as vl_ce_bwd_inplace does with col0 = 0, ncols = V.
+ */
+VL_API vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V,
+                      const uint32_t* labels, int64_t loss_start, int64_t loss_end,
+                      float scale, float* loss, float* lse, float* stats, float* mean,
+                      int32_t* err, void* stream);
+
+/*
+ * Top-k distillation KL with the gradient written in place (train_head.rs: module doc,
+ * kl_rows; the float64 loop of head_kl_matches_host).  Per row t in the window:
+ *     loss[t]     = sum over q with p_q > 0 and col0 <= id_q < col0 + ncols of
+ *                   p_q * (ln p_q - (s[id_q] - lse_t))
+ *     logits[t][j] = (coef + ce_coef) * exp(s_j - lse_t)
+ *                    - coef * sum_{q: id_q = j} p_q - ce_coef * [j == label_t]
+ * for j in [col0, col0 + ncols).  Rows outside the window: loss 0, slice zeroed.
+ *   tid [ntok][k] u32, tp [ntok][k] fp32: the teacher's top-k ids and probabilities,
+ *     taken as given (sum p = 1 is the caller's precondition; repeated ids add up).
+ *   coef: the KL gradient coefficient (the page passes gscale / total).
+ *   Row statistics: from stats_in when not NULL, else lse_in when not NULL, else
+ *     computed here over the full row, which then requires col0 = 0 and ncols = V.
+ *   labels (nullable) with ce_coef folds the CE gradient of the same row into this pass;
+ *     the loss output stays the KL alone.  labels == NULL or ce_coef == 0: KL only.
+ *   loss [ntok] fp32: the KL, or the slice's part of it for a slice (add the parts of
+ *     all slices with vl_acc_add).
+ * k must satisfy 1 <= k <= VL_KL_KMAX.
+ */
+VL_API vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
+                             int64_t col0, int64_t ncols,
+                             const uint32_t* tid, const float* tp, int64_t k, float coef,
+                             int64_t loss_start, int64_t loss_end,
+                             const float* lse_in, const float* stats_in,
+                             const uint32_t* labels, float ce_coef,
+                             float* loss, int32_t* err, void* stream);
+
+/*
+ * Teacher top-k per row (train_head.rs: topk_rows): ids[t][q], q < k, are the columns of
+ * the k largest logits of row t in descending order of value, ties broken by the lower
+ * column (-0.0 equals +0.0); probs[t][q] = exp(s[ids[q]] - s[ids[0]]) / sum over the k.
+ * The selection is exact (the page's per-thread best-8 is not).  Rows outside the window
+ * are not written.  Logits must not hold NaN.  1 <= k <= min(V, VL_TOPK_KMAX).
+ *   ids [ntok][k] u32, probs [ntok][k] fp32.
+ */
+VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
+                       int64_t loss_start, int64_t loss_end,
+                       uint32_t* ids, float* probs, int32_t* err, void* stream);
+
+/*
+ * a[i] = a[i] + b[i] for 0 <= i < n, fp32, bit-exact (train_head.rs: acc_add, which adds a
+ * later vocabulary slice's partial to the first one's).  a and b may not overlap unless
+ * a == b.
+ */
+VL_API vl_status vl_acc_add(float* a, const float* b, int64_t n, void* stream);
+
+/*
+ * Reads (and with clear != 0 resets) the flag that a kernel wait timed out on `device`.
+ * Synchronous: it waits for the device to finish its work.  Returns -1 if the read fails.
+ */
+VL_API int vl_watchdog_flag(int device, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLOSS_H */

@@ -1,0 +1,70 @@
+"""The C-ABI library without a GPU: it loads, exports what include/vloss.h declares,
+and rejects bad arguments on the host before any CUDA call."""
+import pytest
+
+from top_kl_distill_gb300 import vloss as vl
+
+
+def test_library_exports_every_declared_symbol():
+    L = vl.lib()
+    names = vl.declared_symbols()
+    assert {"vl_ce_fwd", "vl_ce_bwd_inplace", "vl_ce_fused", "vl_kl_topk_inplace", "vl_topk_rows",
+            "vl_acc_add"} <= set(names)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert vl.vl_version() >= 100
+    assert L.vl_status_string(1) == b"invalid argument"
+
+
+def _status(fn, *args):
+    with pytest.raises(vl.VlossError) as e:
+        fn(*args)
+    return e.value.status
+
+
+# raw addresses never dereferenced: the host checks reject the call first
+P = 1 << 20
+
+
+def test_rejects_bad_rows():
+    assert _status(vl.vl_ce_fused, P, 10, 4, 11, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, P, 10, 4, 0, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, P, 10, -1, 10, P, 0, 0, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, None, 10, 4, 10, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
+
+
+def test_rejects_bad_windows():
+    assert _status(vl.vl_ce_fwd, P, 10, 4, 10, P, 3, 2, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fwd, P, 10, 4, 10, P, 0, 5, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fwd, P, 10, 4, 10, P, -1, 2, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert "window" in vl.lib().vl_last_error_string().decode()
+
+
+def test_rejects_bad_slices_and_missing_statistics():
+    assert _status(vl.vl_ce_bwd_inplace, P, 10, 4, 10, 6, 5, P, P, None, 0, 4, 1.0, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_bwd_inplace, P, 10, 4, 10, 0, 5, P, None, None, 0, 4, 1.0, None, None, 0) == vl.VL_EINVAL
+    # a KL slice needs the full-row statistics
+    assert _status(vl.vl_kl_topk_inplace, P, 10, 4, 10, 2, 5, P, P, 3, 1.0, 0, 4,
+                   None, None, None, 0.0, P, None, 0) == vl.VL_EINVAL
+
+
+def test_rejects_k_out_of_range():
+    assert _status(vl.vl_kl_topk_inplace, P, 10, 4, 10, 0, 10, P, P, 0, 1.0, 0, 4,
+                   None, None, None, 0.0, P, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_kl_topk_inplace, P, 5000, 4, 5000, 0, 5000, P, P, vl.VL_KL_KMAX + 1, 1.0, 0, 4,
+                   None, None, None, 0.0, P, None, 0) == vl.VL_EUNSUPPORTED
+    assert _status(vl.vl_topk_rows, P, 10, 4, 10, 11, 0, 4, P, P, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_topk_rows, P, 5000, 4, 5000, vl.VL_TOPK_KMAX + 1, 0, 4, P, P, None, 0) == vl.VL_EUNSUPPORTED
+
+
+def test_acc_add_host_checks():
+    assert _status(vl.vl_acc_add, P, P + 16, -1, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_acc_add, P, P + 16, 8, 0) == vl.VL_EINVAL      # overlap: b starts 4 floats into a
+    assert _status(vl.vl_acc_add, None, P, 8, 0) == vl.VL_EINVAL
+    vl.vl_acc_add(P, P + 64, 0, 0)                                     # n = 0 is a no-op
+
+
+def test_empty_calls_launch_nothing():
+    vl.vl_ce_bwd_inplace(P, 10, 0, 10, 0, 10, None, None, None, 0, 0, 1.0, None, None, 0)
+    vl.vl_kl_topk_inplace(P, 10, 0, 10, 0, 10, None, None, 3, 1.0, 0, 0, None, None, None, 0.0, None, None, 0)
+    vl.vl_topk_rows(P, 10, 4, 10, 3, 2, 2, None, None, None, 0)

@@ -1,0 +1,173 @@
+"""Cross-entropy through the C ABI against the oracle (fused, forward, sliced backward)."""
+import zlib
+
+import numpy as np
+import pytest
+
+from oracle import vloss_oracle as O
+from tests import gpu_harness as H
+from top_kl_distill_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _vl():
+    from top_kl_distill_gb300 import vloss
+    return vloss
+
+
+def run_fused(x, lab, ls, le, scale, ld=None, off=0):
+    torch = H.torch_cuda()
+    vl = _vl()
+    ntok, V = x.shape
+    ld = ld or V
+    buf, view = H.strided(x, ld, off)
+    labels = H.dev(lab)
+    loss = torch.full((max(ntok, 1),), -7.0, device="cuda")
+    lse = torch.full((max(ntok, 1),), -7.0, device="cuda")
+    stats = torch.full((max(ntok, 1), 2), -7.0, device="cuda")
+    mean = torch.full((1,), -7.0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vl.vl_ce_fused(view.data_ptr() if ntok else buf.data_ptr(), ld, ntok, V, labels, ls, le, scale, loss, lse,
+                   stats, mean, err)
+    torch.cuda.synchronize()
+    return buf, view, loss, lse, stats, mean, err
+
+
+CASES = {
+    # name: (ntok, V, ld, offset, ls, le, scale, sigma)
+    "tiny_workload": None,
+    "ragged_misaligned": (37, 5003, 5011, 1, 3, 30, 0.25, 3.0),
+    "v1": (6, 1, 1, 0, 0, 6, 1.0, 1.0),
+    "v3_offset2": (9, 3, 5, 2, 1, 8, 0.5, 2.0),
+    "v7": (11, 7, 7, 3, 0, 11, 1.0, 2.0),
+    "v8_ld9": (10, 8, 9, 0, 2, 10, 1.0, 2.0),
+    "cluster_100003": (5, 100003, 100003, 0, 0, 5, 1.0 / 5, 3.0),
+    "empty_window": (12, 777, 777, 0, 5, 5, 1.0, 2.0),
+    "full_window_4tiles": (40, 8192, 8192, 0, 0, 40, 1.0 / 40, 2.0),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_ce_fused(name):
+    if name == "tiny_workload":
+        w = W.WORKLOADS["ce_tiny"]
+        x, lab = W.logits(w), W.labels(w)
+        ls, le, scale, ld, off = w.loss_start, w.loss_end, w.scale, w.V, 0
+    else:
+        ntok, V, ld, off, ls, le, scale, sigma = CASES[name]
+        x = W.random_logits(ntok, V, seed=zlib.crc32(name.encode()), sigma=sigma)
+        lab = W.random_labels(ntok, V, seed=zlib.crc32(name.encode()) + 1)
+    ntok, V = x.shape
+    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
+    oloss, olse, og, omean = O.ce_fused(x, lab, ls, le, scale)
+    g = H.host(view)
+    H.check_grad(g[:, :V], og, scale)
+    if ld > V:
+        assert np.isnan(g[:, V:]).all(), "columns past V were written"
+    if off:
+        assert np.isnan(H.host(buf)[:off]).all(), "memory before the first row was written"
+    H.check_loss(H.host(loss)[:ntok], oloss, olse)
+    H.check_lse(H.host(lse)[:ntok], olse)
+    st = H.host(stats)[:ntok]
+    assert np.array_equal(st[:, 0], x.max(axis=1)), "stats[:, 0] is the exact row max"
+    H.check_lse(st[:, 0].astype(np.float64) + st[:, 1], olse, "m + lnS")
+    H.check_mean(H.host(mean)[0], omean)
+    assert int(H.host(err)[0]) == 0
+
+
+def test_ce_lm_peaky_rows():
+    w = W.WORKLOADS["ce_lm"].scaled(96)
+    w = W.Workload(**{**w.__dict__, "window": (16, 96)})
+    x, lab = W.logits(w), W.labels(w)
+    _, view, loss, lse, _, mean, err = run_fused(x, lab, w.loss_start, w.loss_end, w.scale)
+    oloss, olse, og, omean = O.ce_fused(x, lab, w.loss_start, w.loss_end, w.scale)
+    H.check_grad(H.host(view), og, w.scale)
+    H.check_loss(H.host(loss), oloss, olse)
+    H.check_mean(H.host(mean)[0], omean)
+
+
+def test_ce_zero_rows():
+    torch = H.torch_cuda()
+    vl = _vl()
+    mean = torch.full((1,), 5.0, device="cuda")
+    vl.vl_ce_fused(0, 10, 0, 10, 0, 0, 0, 1.0, 0, None, None, mean, None)
+    torch.cuda.synchronize()
+    assert float(mean[0]) == 0.0
+
+
+def test_ce_bad_labels_counted():
+    ntok, V, ls, le, scale = 20, 3000, 0, 16, 0.5
+    x = W.random_logits(ntok, V, seed=5)
+    lab = W.random_labels(ntok, V, seed=6)
+    lab[[3, 7, 17]] = [V, V + 100, 0xFFFFFFFF]      # rows 3 and 7 in the window, row 17 outside
+    _, view, loss, lse, _, _, err = run_fused(x, lab, ls, le, scale)
+    assert int(H.host(err)[0]) == 2
+    l = H.host(loss)
+    assert np.isnan(l[3]) and np.isnan(l[7]) and l[17] == 0.0
+    fixed = np.where(lab < V, lab, 0).astype(np.uint32)
+    oloss, olse, og, _ = O.ce_fused(x, fixed, ls, le, scale)
+    ok = np.setdiff1d(np.arange(ntok), [3, 7])
+    H.check_loss(l[ok], oloss[ok], olse[ok])
+    g = H.host(view)
+    H.check_grad(g[ok], og[ok], scale)
+    for t in (3, 7):   # a bad label leaves the softmax part of the gradient
+        H.check_grad(g[t], scale * np.exp(x[t].astype(np.float64) - olse[t]), scale)
+
+
+def test_ce_fwd_then_sliced_bwd():
+    torch = H.torch_cuda()
+    vl = _vl()
+    ntok, V, ld, ls, le, scale = 19, 3001, 3007, 2, 17, 1.0 / 15
+    x = W.random_logits(ntok, V, seed=8, sigma=3.0)
+    lab = W.random_labels(ntok, V, seed=9)
+    buf, view = H.strided(x, ld, 2)
+    labels = H.dev(lab)
+    loss = torch.zeros(ntok, device="cuda")
+    lse = torch.zeros(ntok, device="cuda")
+    stats = torch.zeros(ntok, 2, device="cuda")
+    mean = torch.zeros(1, device="cuda")
+    vl.vl_ce_fwd(view.data_ptr(), ld, ntok, V, labels, ls, le, loss, lse, stats, mean, None)
+    parts = []
+    for c0, w in [(0, 1000), (1000, 517), (1517, 1484)]:
+        lp = torch.full((ntok,), -1.0, device="cuda")
+        vl.vl_ce_bwd_inplace(view.data_ptr(), ld, ntok, V, c0, w, labels, None, stats, ls, le, scale, lp, None)
+        parts.append(lp)
+    torch.cuda.synchronize()
+    oloss, olse = O.ce_forward(x, lab, ls, le)
+    og, _ = O.ce_backward(x, lab, olse, ls, le, scale)
+    H.check_loss(H.host(loss), oloss, olse)
+    H.check_lse(H.host(lse), olse)
+    H.check_mean(H.host(mean)[0], O.ce_mean(oloss, ls, le))
+    H.check_grad(H.host(view)[:, :V], og, scale)
+    assert np.isnan(H.host(view)[:, V:]).all()
+    tot = sum(H.host(p).astype(np.float64) for p in parts)
+    H.check_loss(tot, oloss, olse, "sum of slice loss parts")
+
+
+def test_ce_bwd_with_lse_only():
+    torch = H.torch_cuda()
+    vl = _vl()
+    ntok, V, scale = 8, 2500, 0.125
+    x = W.random_logits(ntok, V, seed=10, sigma=1.0)
+    lab = W.random_labels(ntok, V, seed=11)
+    _, olse = O.ce_forward(x, lab, 0, ntok)
+    lse32 = olse.astype(np.float32)
+    xt = H.dev(x)
+    vl.vl_ce_bwd_inplace(xt, V, ntok, V, 0, V, H.dev(lab), H.dev(lse32), None, 0, ntok, scale, None, None)
+    torch.cuda.synchronize()
+    # the oracle given the same fp32 lse (an input of both sides)
+    og, _ = O.ce_backward(x, lab, lse32.astype(np.float64), 0, ntok, scale)
+    H.check_grad(H.host(xt), og, scale)
+
+
+def test_ce_fused_beyond_on_chip_rows():
+    """V past 8 CTAs of staged row: statistics pass + in-place pass through the stats buffer."""
+    ntok, V, scale = 3, 8 * 2048 * 24 + 5, 1.0 / 3
+    x = W.random_logits(ntok, V, seed=12, sigma=2.0)
+    lab = W.random_labels(ntok, V, seed=13)
+    _, view, loss, lse, stats, mean, err = run_fused(x, lab, 0, ntok, scale)
+    oloss, olse, og, omean = O.ce_fused(x, lab, 0, ntok, scale)
+    H.check_grad(H.host(view), og, scale)
+    H.check_loss(H.host(loss), oloss, olse)
+    H.check_mean(H.host(mean)[0], omean)

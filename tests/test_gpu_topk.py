@@ -1,0 +1,73 @@
+"""Teacher top-k through the C ABI against the oracle's full stable sort."""
+import numpy as np
+import pytest
+
+from oracle import vloss_oracle as O
+from tests import gpu_harness as H
+from top_kl_distill_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def run_topk(x, k, ls=0, le=None, ld=None, off=0):
+    torch = H.torch_cuda()
+    from top_kl_distill_gb300 import vloss as vl
+    ntok, V = x.shape
+    le = ntok if le is None else le
+    ld = ld or V
+    _, view = H.strided(x, ld, off)
+    ids = torch.full((ntok, k), -1, dtype=torch.int32, device="cuda")
+    probs = torch.full((ntok, k), -1.0, device="cuda")
+    vl.vl_topk_rows(view.data_ptr(), ld, ntok, V, k, ls, le, ids, probs)
+    torch.cuda.synchronize()
+    return H.host(ids).view(np.uint32), H.host(probs)
+
+
+def check(x, k, ls=0, le=None, **kw):
+    ntok = x.shape[0]
+    le = ntok if le is None else le
+    ids, probs = run_topk(x, k, ls, le, **kw)
+    oids, oprobs, valid = O.topk_rows(x, k, ls, le)
+    assert np.array_equal(ids[valid].astype(np.int64), oids[valid]), "top-k ids differ"
+    H.check_probs(probs[valid], oprobs[valid])
+    assert np.all(ids[~valid] == 0xFFFFFFFF) and np.all(probs[~valid] == -1.0), "rows outside the window written"
+
+
+@pytest.mark.parametrize("k", [256, 2048])
+def test_topk_workload_rows(k):
+    w = W.WORKLOADS["topk"].scaled(6)
+    check(W.logits(w), k)
+
+
+@pytest.mark.parametrize("k", [1, 7, 100, 700])
+def test_topk_tie_heavy(k):
+    check(W.tie_heavy_logits(16, 3000, seed=k), k)
+
+
+def test_topk_all_equal_and_signed_zeros():
+    x = np.zeros((3, 5000), dtype=np.float32)
+    x[1, ::2] = -0.0
+    x[2] = 1.5
+    check(x, 50)
+    check(x, 2048)
+
+
+def test_topk_monotone_rows():
+    """Ascending rows admit every new column (the most compactions); descending rows almost none."""
+    V = 50000
+    up = np.arange(V, dtype=np.float32)[None, :] * np.float32(1e-3)
+    x = np.concatenate([up, up[:, ::-1].copy(), -up], axis=0)
+    for k in (1, 256, 2048):
+        check(x, k)
+
+
+def test_topk_k_equals_v_and_misaligned():
+    x = W.random_logits(5, 1500, seed=3)
+    check(x, 1500)
+    x = W.random_logits(11, 6007, seed=4)
+    check(x, 333, ls=2, le=9, ld=6011, off=1)
+
+
+def test_topk_window_only():
+    x = W.random_logits(10, 4000, seed=5)
+    check(x, 64, ls=3, le=7)

@@ -1,0 +1,255 @@
+// Device-side building blocks shared by the libvloss kernels (sm_103a).
+//
+// Inline PTX for what the CUDA C++ front end does not expose directly:
+// mbarriers with transaction counts, 1-D bulk copies global -> shared
+// (cp.async.bulk, the TMA engine's untiled form), cluster ranks and
+// distributed shared memory, named barriers with a popcount, and the
+// global nanosecond timer used to bound every wait.
+#pragma once
+
+#include <cstdint>
+#include <cfloat>
+#include <cuda_runtime.h>
+
+namespace vl {
+
+// A wait that has not completed after this long is a bug: the kernel records it
+// and unwinds instead of hanging the GPU.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// 2^x on the special-function unit (ex2.approx, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init_cluster() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Acquire at cluster scope: pairs with a remote release-arrive from a peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false if the wait gave up: either another thread of the CTA raised
+// *abort, or this wait ran past kWaitTimeoutNs (then it raises *abort and sets
+// *flag).  Every wait in the library goes through here.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            unsigned int* flag) {
+    const uint32_t b = smem_u32(bar);
+    if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                *abort = 1;
+                atomicOr(flag, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// Same wait without the abort check, for draining copies already in flight.
+__device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ bulk copy
+
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is signalled on `bar`
+// as a transaction count.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// ------------------------------------------------------------------ cluster
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ncluster_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(a) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(bar_cluster_addr) : "memory");
+}
+
+// ------------------------------------------------------------------ CTA-level
+
+// Named barrier `id` over `n` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also returns how many participating threads passed pred = true.
+__device__ __forceinline__ uint32_t named_sync_popc(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.u32 p, %3, 0;\n\t"
+                 "bar.red.popc.u32 %0, %1, %2, p;\n\t}"
+                 : "=r"(r) : "r"(id), "r"(n), "r"((uint32_t)pred) : "memory");
+    return r;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue; it still waits for this grid's memory before reading it.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ stores / loads
+
+__device__ __forceinline__ void st_global_v4(float* p, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(const float* p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(smem_u32(p)));
+    return v;
+}
+
+// ------------------------------------------------------------------ online softmax statistics
+
+// Running (max, sum of exp(x - max)) of a stream of values.
+struct MaxSum {
+    float m;
+    float s;
+};
+
+__device__ __forceinline__ MaxSum ms_empty() { return MaxSum{-FLT_MAX, 0.0f}; }
+
+__device__ __forceinline__ void ms_add(MaxSum& a, float x) {
+    if (x > a.m) {
+        a.s = a.s * ex2((a.m - x) * kLog2e);
+        a.m = x;
+    }
+    a.s += ex2((x - a.m) * kLog2e);
+}
+
+__device__ __forceinline__ void ms_add4(MaxSum& a, float4 v) {
+    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mx > a.m) {
+        a.s = a.s * ex2((a.m - mx) * kLog2e);
+        a.m = mx;
+    }
+    a.s += (ex2((v.x - a.m) * kLog2e) + ex2((v.y - a.m) * kLog2e)) +
+           (ex2((v.z - a.m) * kLog2e) + ex2((v.w - a.m) * kLog2e));
+}
+
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
+    const float m = fmaxf(a.m, b.m);
+    return MaxSum{m, a.s * ex2((a.m - m) * kLog2e) + b.s * ex2((b.m - m) * kLog2e)};
+}
+
+__device__ __forceinline__ MaxSum ms_warp_reduce(MaxSum a) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        MaxSum b{__shfl_xor_sync(0xffffffffu, a.m, off), __shfl_xor_sync(0xffffffffu, a.s, off)};
+        a = ms_merge(a, b);
+    }
+    return a;
+}
+
+__device__ __forceinline__ float warp_sum(float a) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    return a;
+}
+
+}  // namespace vl

@@ -1,0 +1,53 @@
+// Internal interface between the C ABI (vloss_api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vl {
+
+// Work of one row-engine launch.  Column indices are relative to col0.
+struct RowParams {
+    float* x;                 // logits, column 0 of row 0
+    long long ld, ntok, V, col0, ncols;
+    const uint32_t* labels;   // CE ops; KL fold (nullable)
+    const uint32_t* tid;      // KL teacher ids [ntok][k]
+    const float* tp;          // KL teacher probabilities [ntok][k]
+    int k;
+    float cg;                 // multiplier of softmax in the gradient
+    float coef;               // KL: teacher scatter coefficient
+    float ce_coef;            // one-hot subtraction coefficient (0: none)
+    long long ls, le;         // loss window
+    const float* lse_in;      // given row statistics (stats_in wins)
+    const float* stats_in;
+    float* loss;              // per-row loss (CE loss / KL / CE loss part)
+    float* lse_out;
+    float* stats_out;
+    int* err;
+    int csize;                // CTAs per row (cluster size)
+};
+
+enum RowOp : int { kCeFused = 0, kCeFwd = 1, kCeBwd = 2, kKl = 3 };
+
+// Row-engine geometry limits (rows.cu).
+constexpr int kTileF = 2048;              // floats per pipeline tile (8 KB)
+constexpr int kSlots = 24;                // tiles in the shared-memory ring
+constexpr int kMaxCluster = 8;
+constexpr long long kResidentMax = (long long)kSlots * kTileF;   // floats of one row part held on chip
+
+// Launch `op` over P; `resident` selects the mode that computes the row statistics
+// from the staged row (CE fused, self-contained KL).  Returns a CUDA error code.
+cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters, cudaStream_t st);
+
+// Max active clusters of size c for the row kernel of `op` on the current device.
+int row_max_clusters(int op, bool resident, int c);
+
+unsigned int rows_watchdog(bool clear);
+
+// Top-k (topk.cu).
+cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long V, int k,
+                        long long ls, long long le, uint32_t* ids, float* probs, int* err,
+                        cudaStream_t st);
+unsigned int topk_watchdog(bool clear);
+
+}  // namespace vl

@@ -1,0 +1,411 @@
+// C ABI of libvloss: argument checks on the host, launch choice, small kernels
+// (acc_add, windowed mean).  Declarations and contracts: include/vloss.h.
+#include "vl_device.cuh"
+#include "vl_internal.h"
+#include "../../include/vloss.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+namespace vl {
+namespace {
+
+thread_local std::string g_last_error;
+
+vl_status fail(vl_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+vl_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(VL_ELAUNCH, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+vl_status ok() { return VL_OK; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+constexpr long long kMaxCols = 0x7fffffffLL;   // ids and labels are uint32 columns
+
+vl_status check_rows(const void* logits, int64_t ld, int64_t ntok, int64_t V, const char* fn) {
+    if (ntok < 0) return fail(VL_EINVAL, "%s: ntok < 0", fn);
+    if (V < 1 || V > kMaxCols) return fail(VL_EINVAL, "%s: V must be in [1, 2^31)", fn);
+    if (ld < V) return fail(VL_EINVAL, "%s: ld (%lld) < V (%lld)", fn, (long long)ld, (long long)V);
+    if (ntok > 0 && logits == nullptr) return fail(VL_EINVAL, "%s: logits is NULL", fn);
+    return ok();
+}
+
+vl_status check_window(int64_t ls, int64_t le, int64_t ntok, const char* fn) {
+    if (!(0 <= ls && ls <= le && le <= ntok))
+        return fail(VL_EINVAL, "%s: window [%lld, %lld) not inside [0, %lld]", fn, (long long)ls, (long long)le,
+                    (long long)ntok);
+    return ok();
+}
+
+vl_status check_slice(int64_t col0, int64_t ncols, int64_t V, const char* fn) {
+    if (col0 < 0 || ncols < 0 || col0 + ncols > V)
+        return fail(VL_EINVAL, "%s: slice [%lld, %lld) not inside [0, %lld)", fn, (long long)col0,
+                    (long long)(col0 + ncols), (long long)V);
+    return ok();
+}
+
+int num_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+// Cluster size for a resident-mode launch: the smallest that fits a row part on
+// chip, raised while the estimated time (rows per cluster x part length, plus a
+// fixed per-row cost for the exchange) drops.  VLOSS_CLUSTER=c overrides it.
+struct Grid {
+    int csize;
+    int nclusters;
+};
+
+Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
+    const int sms = num_sms();
+    if (!resident) {
+        long long g = rows < sms ? rows : sms;
+        return Grid{1, (int)(g > 0 ? g : 1)};
+    }
+    const long long body = ncols;   // upper bound of the aligned body
+    int cmin = (int)((body + kResidentMax - 1) / kResidentMax);
+    if (cmin < 1) cmin = 1;
+    if (cmin > kMaxCluster) return Grid{0, 0};
+    int forced = 0;
+    if (const char* e = std::getenv("VLOSS_CLUSTER")) forced = std::atoi(e);
+    if (forced >= cmin && forced <= kMaxCluster) {
+        const int n = row_max_clusters(op, resident, forced);
+        if (n > 0) return Grid{forced, (int)(rows < n ? rows : n)};
+    }
+    Grid best{0, 0};
+    double best_cost = 0;
+    for (int c = cmin; c <= kMaxCluster; ++c) {
+        const int n = row_max_clusters(op, resident, c);
+        if (n <= 0) continue;
+        const long long ncl = rows < n ? rows : n;
+        const long long waves = (rows + ncl - 1) / ncl;
+        const double part = (double)((ncols + c - 1) / c);
+        const double cost = (double)waves * (part + (c > 1 ? (double)kTileF : 0.0));
+        if (best.csize == 0 || cost < best_cost * 0.98) {
+            best = Grid{c, (int)(ncl > 0 ? ncl : 1)};
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// ------------------------------------------------------------------ small kernels
+
+__global__ void acc_add_kernel(float* a, const float* b, long long head, long long n4,
+                               long long n) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    if (tid < head) a[tid] = a[tid] + b[tid];
+    float4* a4 = reinterpret_cast<float4*>(a + head);
+    const float4* b4 = reinterpret_cast<const float4*>(b + head);
+    for (long long i = tid; i < n4; i += stride) {
+        float4 x = a4[i];
+        const float4 y = b4[i];
+        x.x = x.x + y.x;
+        x.y = x.y + y.y;
+        x.z = x.z + y.z;
+        x.w = x.w + y.w;
+        a4[i] = x;
+    }
+    const long long t0 = head + 4 * n4;
+    if (t0 + tid < n) a[t0 + tid] = a[t0 + tid] + b[t0 + tid];
+}
+
+__global__ void acc_add_scalar_kernel(float* a, const float* b, long long n) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) a[i] = a[i] + b[i];
+}
+
+// mean of loss[ls, le), summed in double in a fixed order.  Launched as a
+// programmatic dependent of the loss kernel: its launch overlaps that kernel,
+// griddepcontrol.wait holds it until the losses are in memory.
+__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ loss, long long ls, long long le,
+                                                    float* __restrict__ mean) {
+    pdl_wait_primary();
+    __shared__ double red[32];
+    double acc = 0.0;
+    for (long long i = ls + threadIdx.x; i < le; i += blockDim.x) acc += (double)loss[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+        *mean = le > ls ? (float)(s / (double)(le - ls)) : 0.0f;
+    }
+}
+
+cudaError_t launch_mean(const float* loss, long long ls, long long le, float* mean, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(1024, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {(void*)&loss, (void*)&ls, (void*)&le, (void*)&mean};
+    return cudaLaunchKernelExC(&cfg, (const void*)mean_kernel, args);
+}
+
+RowParams base_params(float* logits, int64_t ld, int64_t ntok, int64_t V) {
+    RowParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.x = logits;
+    P.ld = ld;
+    P.ntok = ntok;
+    P.V = V;
+    P.col0 = 0;
+    P.ncols = V;
+    P.csize = 1;
+    return P;
+}
+
+vl_status run_rows(int op, bool resident, RowParams& P, long long rows, const char* fn, cudaStream_t st) {
+    const Grid g = choose_grid(op, resident, rows, P.ncols);
+    if (g.csize == 0)
+        return fail(VL_EUNSUPPORTED, "%s: a row of %lld columns does not fit %d CTAs of %lld floats", fn,
+                    (long long)P.ncols, kMaxCluster, (long long)kResidentMax);
+    P.csize = g.csize;
+    const cudaError_t e = launch_rows(op, resident, P, g.nclusters, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+}  // namespace
+}  // namespace vl
+
+using namespace vl;
+
+extern "C" {
+
+int vl_version(void) { return 100; }
+
+const char* vl_status_string(vl_status s) {
+    switch (s) {
+        case VL_OK: return "ok";
+        case VL_EINVAL: return "invalid argument";
+        case VL_ELAUNCH: return "CUDA launch or runtime error";
+        case VL_EUNSUPPORTED: return "unsupported by this build";
+    }
+    return "unknown status";
+}
+
+const char* vl_last_error_string(void) { return g_last_error.c_str(); }
+
+vl_status vl_ce_fwd(const float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                    int64_t loss_start, int64_t loss_end, float* loss, float* lse, float* stats, float* mean,
+                    int32_t* err, void* stream) {
+    const char* fn = "vl_ce_fwd";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
+    const cudaStream_t st = as_stream(stream);
+    if (ntok > 0) {
+        RowParams P = base_params(const_cast<float*>(logits), ld, ntok, V);
+        P.labels = labels;
+        P.ls = loss_start;
+        P.le = loss_end;
+        P.loss = loss;
+        P.lse_out = lse;
+        P.stats_out = stats;
+        P.err = err;
+        if ((s = run_rows(kCeFwd, false, P, ntok, fn, st))) return s;
+    }
+    if (mean) {
+        const cudaError_t e = launch_mean(loss, loss_start, loss_end, mean, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return VL_OK;
+}
+
+vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                            const uint32_t* labels, const float* lse, const float* stats, int64_t loss_start,
+                            int64_t loss_end, float scale, float* loss_part, int32_t* err, void* stream) {
+    const char* fn = "vl_ce_bwd_inplace";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if ((s = check_slice(col0, ncols, V, fn))) return s;
+    if (ntok > 0 && labels == nullptr) return fail(VL_EINVAL, "%s: labels is NULL", fn);
+    if (ntok > 0 && lse == nullptr && stats == nullptr) return fail(VL_EINVAL, "%s: need lse or stats", fn);
+    if (ntok == 0 || ncols == 0) return VL_OK;
+    RowParams P = base_params(logits, ld, ntok, V);
+    P.col0 = col0;
+    P.ncols = ncols;
+    P.labels = labels;
+    P.lse_in = lse;
+    P.stats_in = stats;
+    P.ls = loss_start;
+    P.le = loss_end;
+    P.cg = scale;
+    P.ce_coef = scale;
+    P.loss = loss_part;
+    P.err = err;
+    return run_rows(kCeBwd, false, P, ntok, fn, as_stream(stream));
+}
+
+vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                      int64_t loss_start, int64_t loss_end, float scale, float* loss, float* lse, float* stats,
+                      float* mean, int32_t* err, void* stream) {
+    const char* fn = "vl_ce_fused";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
+    const cudaStream_t st = as_stream(stream);
+    if (ntok > 0) {
+        if (V > (long long)kMaxCluster * kResidentMax) {
+            // too long to stage on chip: statistics pass, then the in-place pass
+            if (stats == nullptr)
+                return fail(VL_EUNSUPPORTED, "%s: V > %lld needs the stats buffer", fn,
+                            (long long)kMaxCluster * kResidentMax);
+            if ((s = vl_ce_fwd(logits, ld, ntok, V, labels, loss_start, loss_end, loss, lse, stats, nullptr, err,
+                               stream)))
+                return s;
+            if ((s = vl_ce_bwd_inplace(logits, ld, ntok, V, 0, V, labels, nullptr, stats, loss_start, loss_end,
+                                       scale, nullptr, nullptr, stream)))
+                return s;
+        } else {
+            RowParams P = base_params(logits, ld, ntok, V);
+            P.labels = labels;
+            P.ls = loss_start;
+            P.le = loss_end;
+            P.cg = scale;
+            P.ce_coef = scale;
+            P.loss = loss;
+            P.lse_out = lse;
+            P.stats_out = stats;
+            P.err = err;
+            if ((s = run_rows(kCeFused, true, P, ntok, fn, st))) return s;
+        }
+    }
+    if (mean) {
+        const cudaError_t e = launch_mean(loss, loss_start, loss_end, mean, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return VL_OK;
+}
+
+vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                             const uint32_t* tid, const float* tp, int64_t k, float coef, int64_t loss_start,
+                             int64_t loss_end, const float* lse_in, const float* stats_in, const uint32_t* labels,
+                             float ce_coef, float* loss, int32_t* err, void* stream) {
+    const char* fn = "vl_kl_topk_inplace";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if ((s = check_slice(col0, ncols, V, fn))) return s;
+    if (k < 1) return fail(VL_EINVAL, "%s: k < 1", fn);
+    if (k > VL_KL_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_KL_KMAX);
+    if (ntok > 0 && (tid == nullptr || tp == nullptr || loss == nullptr))
+        return fail(VL_EINVAL, "%s: tid, tp or loss is NULL", fn);
+    const bool self = lse_in == nullptr && stats_in == nullptr;
+    if (self && (col0 != 0 || ncols != V))
+        return fail(VL_EINVAL, "%s: a slice needs lse_in or stats_in (the statistics of the full row)", fn);
+    if (ntok == 0) return VL_OK;
+    RowParams P = base_params(logits, ld, ntok, V);
+    P.col0 = col0;
+    P.ncols = ncols;
+    P.tid = tid;
+    P.tp = tp;
+    P.k = (int)k;
+    const bool fold = labels != nullptr && ce_coef != 0.0f;
+    P.labels = fold ? labels : nullptr;
+    P.ce_coef = fold ? ce_coef : 0.0f;
+    P.coef = coef;
+    P.cg = coef + P.ce_coef;
+    P.ls = loss_start;
+    P.le = loss_end;
+    P.lse_in = lse_in;
+    P.stats_in = stats_in;
+    P.loss = loss;
+    P.err = err;
+    if (self && V > (long long)kMaxCluster * kResidentMax)
+        return fail(VL_EUNSUPPORTED, "%s: V > %lld: compute stats with vl_ce_fwd and pass stats_in", fn,
+                    (long long)kMaxCluster * kResidentMax);
+    const long long rows = loss_end - loss_start;
+    return run_rows(kKl, self, P, rows > 0 ? rows : 1, fn, as_stream(stream));
+}
+
+vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k, int64_t loss_start,
+                       int64_t loss_end, uint32_t* ids, float* probs, int32_t* err, void* stream) {
+    const char* fn = "vl_topk_rows";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (k < 1 || k > V) return fail(VL_EINVAL, "%s: k = %lld outside [1, V]", fn, (long long)k);
+    if (k > VL_TOPK_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_TOPK_KMAX);
+    if (loss_end > loss_start && (ids == nullptr || probs == nullptr))
+        return fail(VL_EINVAL, "%s: ids or probs is NULL", fn);
+    if (loss_end == loss_start) return VL_OK;
+    const cudaError_t e = launch_topk(logits, ld, ntok, V, (int)k, loss_start, loss_end, ids, probs, err,
+                                      as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
+vl_status vl_acc_add(float* a, const float* b, int64_t n, void* stream) {
+    const char* fn = "vl_acc_add";
+    if (n < 0) return fail(VL_EINVAL, "%s: n < 0", fn);
+    if (n == 0) return VL_OK;
+    if (a == nullptr || b == nullptr) return fail(VL_EINVAL, "%s: NULL pointer", fn);
+    if (a != b && ((a < b && a + n > b) || (b < a && b + n > a)))
+        return fail(VL_EINVAL, "%s: a and b overlap", fn);
+    const cudaStream_t st = as_stream(stream);
+    const int sms = num_sms();
+    const uintptr_t ma = reinterpret_cast<uintptr_t>(a) & 15u, mb = reinterpret_cast<uintptr_t>(b) & 15u;
+    if (ma == mb && (ma & 3u) == 0) {
+        long long head = (long long)((16u - ma) & 15u) / 4;
+        if (head > n) head = n;
+        const long long n4 = (n - head) / 4;
+        long long blocks = (n4 + 255) / 256;
+        const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        acc_add_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, b, head, n4, n);
+    } else {
+        long long blocks = (n + 255) / 256;
+        const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+        if (blocks > cap) blocks = cap;
+        acc_add_scalar_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, b, n);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
+int vl_watchdog_flag(int device, int clear) {
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return -1;
+    if (cudaSetDevice(device) != cudaSuccess) return -1;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaSetDevice(prev);
+        return -1;
+    }
+    const unsigned int a = rows_watchdog(clear != 0), b = topk_watchdog(clear != 0);
+    cudaSetDevice(prev);
+    if (a == 0xffffffffu || b == 0xffffffffu) return -1;
+    return (int)((a | b) & 0x7fffffffu);
+}
+
+}  // extern "C"

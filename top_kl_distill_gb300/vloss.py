@@ -1,0 +1,158 @@
+"""Python binding of libvloss: the C entry points under the same names.
+
+Argument marshalling only: every step runs in the CUDA library.  Each pointer
+parameter accepts a torch tensor (its data pointer is passed after a dtype
+and device check), a raw integer device address, or None for NULL.  ``stream``
+accepts a torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's
+current stream on the current device.  A status other than VL_OK raises
+VlossError with the library's message.
+
+The library must have been built in-tree (``python -m top_kl_distill_gb300.build``
+or ``__graft_entry__.build()``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libvloss.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "vloss.h")
+
+VL_OK, VL_EINVAL, VL_ELAUNCH, VL_EUNSUPPORTED = 0, 1, 2, 3
+VL_KL_KMAX = 1024
+VL_TOPK_KMAX = 2048
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_F = ctypes.c_float
+
+_SIGS = {
+    "vl_ce_fwd": [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P],
+    "vl_ce_bwd_inplace": [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P],
+    "vl_ce_fused": [_P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _P, _P, _P, _P],
+    "vl_kl_topk_inplace": [_P, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _I, _P, _P, _P, _F, _P, _P, _P],
+    "vl_topk_rows": [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P],
+    "vl_acc_add": [_P, _P, _I, _P],
+}
+
+_lib = None
+
+
+class VlossError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} -> status {status}: {msg}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libvloss.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m top_kl_distill_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.vl_version.restype = ctypes.c_int
+        L.vl_status_string.restype = ctypes.c_char_p
+        L.vl_status_string.argtypes = [ctypes.c_int]
+        L.vl_last_error_string.restype = ctypes.c_char_p
+        L.vl_watchdog_flag.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.vl_watchdog_flag.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/vloss.h declares."""
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(vl_\w+)\s*\(", txt, flags=re.M)))
+
+
+_DT = {"f32": "torch.float32", "u32": "torch.uint32", "i32": "torch.int32"}
+
+
+def _ptr(x, kind: str, name: str):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a tensor, an int address or None")
+    if not x.is_cuda:
+        raise ValueError(f"{name}: tensor must live on a CUDA device")
+    want = {"f32": (torch.float32,), "u32": (torch.uint32, torch.int32), "i32": (torch.int32,)}[kind]
+    if x.dtype not in want:
+        raise TypeError(f"{name}: dtype {x.dtype}, expected {_DT[kind]}")
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != VL_OK:
+        msg = lib().vl_last_error_string().decode()
+        raise VlossError(fn, status, msg)
+
+
+def vl_version() -> int:
+    return lib().vl_version()
+
+
+def vl_ce_fwd(logits, ld, ntok, V, labels, loss_start, loss_end, loss, lse=None, stats=None, mean=None,
+              err=None, stream=None):
+    _check("vl_ce_fwd", lib().vl_ce_fwd(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, _ptr(labels, "u32", "labels"), loss_start, loss_end,
+        _ptr(loss, "f32", "loss"), _ptr(lse, "f32", "lse"), _ptr(stats, "f32", "stats"),
+        _ptr(mean, "f32", "mean"), _ptr(err, "i32", "err"), _stream(stream)))
+
+
+def vl_ce_bwd_inplace(logits, ld, ntok, V, col0, ncols, labels, lse, stats, loss_start, loss_end, scale,
+                      loss_part=None, err=None, stream=None):
+    _check("vl_ce_bwd_inplace", lib().vl_ce_bwd_inplace(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, col0, ncols, _ptr(labels, "u32", "labels"),
+        _ptr(lse, "f32", "lse"), _ptr(stats, "f32", "stats"), loss_start, loss_end, float(scale),
+        _ptr(loss_part, "f32", "loss_part"), _ptr(err, "i32", "err"), _stream(stream)))
+
+
+def vl_ce_fused(logits, ld, ntok, V, labels, loss_start, loss_end, scale, loss, lse=None, stats=None,
+                mean=None, err=None, stream=None):
+    _check("vl_ce_fused", lib().vl_ce_fused(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, _ptr(labels, "u32", "labels"), loss_start, loss_end,
+        float(scale), _ptr(loss, "f32", "loss"), _ptr(lse, "f32", "lse"), _ptr(stats, "f32", "stats"),
+        _ptr(mean, "f32", "mean"), _ptr(err, "i32", "err"), _stream(stream)))
+
+
+def vl_kl_topk_inplace(logits, ld, ntok, V, col0, ncols, tid, tp, k, coef, loss_start, loss_end,
+                       lse_in=None, stats_in=None, labels=None, ce_coef=0.0, loss=None, err=None, stream=None):
+    _check("vl_kl_topk_inplace", lib().vl_kl_topk_inplace(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, col0, ncols, _ptr(tid, "u32", "tid"), _ptr(tp, "f32", "tp"),
+        k, float(coef), loss_start, loss_end, _ptr(lse_in, "f32", "lse_in"), _ptr(stats_in, "f32", "stats_in"),
+        _ptr(labels, "u32", "labels"), float(ce_coef), _ptr(loss, "f32", "loss"), _ptr(err, "i32", "err"),
+        _stream(stream)))
+
+
+def vl_topk_rows(logits, ld, ntok, V, k, loss_start, loss_end, ids, probs, err=None, stream=None):
+    _check("vl_topk_rows", lib().vl_topk_rows(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, k, loss_start, loss_end, _ptr(ids, "u32", "ids"),
+        _ptr(probs, "f32", "probs"), _ptr(err, "i32", "err"), _stream(stream)))
+
+
+def vl_acc_add(a, b, n, stream=None):
+    _check("vl_acc_add", lib().vl_acc_add(_ptr(a, "f32", "a"), _ptr(b, "f32", "b"), n, _stream(stream)))
+
+
+def vl_watchdog_flag(device: int = 0, clear: bool = True) -> int:
+    return lib().vl_watchdog_flag(device, 1 if clear else 0)
