@@ -1,0 +1,661 @@
+"""Benchmark of the fused vocabulary-row losses on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-sweep]
+    python bench.py --impl reference ...      # the CPU oracle arm
+
+Headline workload: fused cross-entropy over 512 token rows x 32000 vocabulary
+fp32 logits, window [128, 512), scale 1/384 -- one step is one vl_ce_fused call
+(loss, lse, in-place gradient, windowed mean) over the whole batch.  `value` is
+token-rows per second over all ranks; each rank runs its own copy of the batch
+(rows are independent, so ranks share no data and scaling is weak).
+
+Timing: every timed step reads a freshly restored copy of the pristine inputs
+(the kernels overwrite the logits with the gradient).  Restores happen outside
+the events, followed by a write of a buffer larger than L2, so every step
+starts with a cold L2.  CUDA events on the launching stream bracket each step;
+the dominant kernel is also timed alone, launch by launch, for the roofline.
+
+The sweep (on by default) measures the other workloads the same way and
+reports them under "sweep": top-k KL 2048 x 32000 (k 64), teacher top-k
+4096 x 128256 (k 256 and 2048), and the large-vocabulary step 8192 x 128256
+(CE forward, two vocabulary slices of KL + CE gradient, acc_add).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from top_kl_distill_gb300 import workloads as W  # noqa: E402
+from top_kl_distill_gb300.slicing import cuts_for_slices  # noqa: E402
+
+METRIC = "token-rows/sec and achieved HBM GB/s (% of GB300 peak) at 32000/128256 vocab"
+UNIT = "token-rows/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the loop runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+
+class Case:
+    """One workload: pristine inputs on the device, R work buffers, step and kernel calls."""
+
+    name = ""
+    inplace = True
+    launches_per_step = 1
+
+    def rows(self) -> int:
+        raise NotImplementedError
+
+    def bytes_per_step(self) -> int:
+        raise NotImplementedError
+
+
+def _dev(torch, a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        return torch.from_numpy(a.view(np.int32)).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+class CeFused(Case):
+    def __init__(self, torch, w, nbuf):
+        from top_kl_distill_gb300 import vloss as vl
+        self.vl, self.w, self.torch = vl, w, torch
+        self.name = w.name
+        self.launches_per_step = 2          # fused kernel + windowed mean
+        self.x_host = W.logits(w)
+        self.lab_host = W.labels(w)
+        self.pristine = _dev(torch, self.x_host)
+        self.labels = _dev(torch, self.lab_host)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+        n = w.ntok
+        self.loss = torch.zeros(n, device="cuda")
+        self.lse = torch.zeros(n, device="cuda")
+        self.mean = torch.zeros(1, device="cuda")
+
+    def rows(self):
+        return self.w.ntok
+
+    def bytes_per_step(self):
+        # per row: read and write V fp32, read the label, write loss and lse; plus the mean
+        return self.w.ntok * (8 * self.w.V + 12) + (self.w.loss_end - self.w.loss_start) * 4 + 4
+
+    def kernel_bytes(self):
+        return self.w.ntok * (8 * self.w.V + 12)
+
+    def restore(self, j):
+        self.bufs[j].copy_(self.pristine)
+
+    def step(self, j, mean=True):
+        w = self.w
+        self.vl.vl_ce_fused(self.bufs[j], w.V, w.ntok, w.V, self.labels, w.loss_start, w.loss_end, w.scale,
+                            self.loss, self.lse, None, self.mean if mean else None, None)
+
+    def kernel(self, j):
+        self.step(j, mean=False)
+
+
+class Kl(Case):
+    def __init__(self, torch, w, nbuf):
+        from top_kl_distill_gb300 import vloss as vl
+        self.vl, self.w = vl, w
+        self.name = w.name
+        self.pristine = _dev(torch, W.logits(w))
+        tid, tp = W.teacher(w)
+        self.tid, self.tp = _dev(torch, tid), _dev(torch, tp)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+        self.loss = torch.zeros(w.ntok, device="cuda")
+
+    def rows(self):
+        return self.w.ntok
+
+    def bytes_per_step(self):
+        return self.w.ntok * (8 * self.w.V + 8 * self.w.k + 4)
+
+    kernel_bytes = bytes_per_step
+
+    def restore(self, j):
+        self.bufs[j].copy_(self.pristine)
+
+    def step(self, j):
+        w = self.w
+        self.vl.vl_kl_topk_inplace(self.bufs[j], w.V, w.ntok, w.V, 0, w.V, self.tid, self.tp, w.k, w.coef,
+                                   w.loss_start, w.loss_end, None, None, None, 0.0, self.loss, None)
+
+    kernel = step
+
+
+class TopK(Case):
+    inplace = False
+    _cache = {}
+
+    def __init__(self, torch, w, nbuf, k):
+        from top_kl_distill_gb300 import vloss as vl
+        self.vl, self.w, self.k = vl, w, k
+        self.name = f"{w.name}_k{k}"
+        key = (w.name, w.ntok)
+        if TopK._cache.get("key") != key:
+            TopK._cache.clear()
+            TopK._cache.update(key=key, x=_dev(torch, W.logits(w)))
+        self.x = TopK._cache["x"]
+        self.bufs = [self.x]
+        self.ids = torch.zeros((w.ntok, k), dtype=torch.int32, device="cuda")
+        self.probs = torch.zeros((w.ntok, k), device="cuda")
+
+    def rows(self):
+        return self.w.ntok
+
+    def bytes_per_step(self):
+        return self.w.ntok * (4 * self.w.V + 8 * self.k)
+
+    kernel_bytes = bytes_per_step
+
+    def restore(self, j):
+        pass
+
+    def step(self, j):
+        w = self.w
+        self.vl.vl_topk_rows(self.x, w.V, w.ntok, w.V, self.k, 0, w.ntok, self.ids, self.probs)
+
+    kernel = step
+
+
+class LargeV(Case):
+    """CE forward over full rows, then per vocabulary slice the in-place KL + CE gradient
+    from the row statistics, then acc_add of the slices' KL parts."""
+
+    def __init__(self, torch, w, nbuf):
+        from top_kl_distill_gb300 import vloss as vl
+        self.vl, self.w = vl, w
+        self.name = w.name
+        self.launches_per_step = 2 + w.slices
+        self.pristine = _dev(torch, W.logits(w))
+        self.labels = _dev(torch, W.labels(w))
+        tid, tp = W.teacher(w)
+        self.tid, self.tp = _dev(torch, tid), _dev(torch, tp)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+        n = w.ntok
+        self.ce_loss = torch.zeros(n, device="cuda")
+        self.lse = torch.zeros(n, device="cuda")
+        self.stats = torch.zeros((n, 2), device="cuda")
+        self.mean = torch.zeros(1, device="cuda")
+        self.parts = [torch.zeros(n, device="cuda") for _ in range(w.slices)]
+        self.cuts = cuts_for_slices(w.V, w.slices)
+
+    def rows(self):
+        return self.w.ntok
+
+    def bytes_per_step(self):
+        w = self.w
+        fwd = 4 * w.V + 4 + 4 + 4 + 8                     # row, label, loss, lse, stats
+        per_slice = 8 * (w.V // w.slices) + 8 * w.k + 4 + 8 + 4   # slice rw, support, label, stats, part
+        acc = 12 * (w.slices - 1)
+        return w.ntok * (fwd + w.slices * per_slice + acc) + w.ntok * 4 + 4
+
+    def kernel_bytes(self):
+        w = self.w
+        return w.ntok * (8 * self.cuts[0][1] + 8 * w.k + 4 + 8 + 4)
+
+    def restore(self, j):
+        self.bufs[j].copy_(self.pristine)
+
+    def step(self, j):
+        w, vl, x = self.w, self.vl, self.bufs[j]
+        vl.vl_ce_fwd(x, w.V, w.ntok, w.V, self.labels, 0, w.ntok, self.ce_loss, self.lse, self.stats, self.mean,
+                     None)
+        for (c0, width), part in zip(self.cuts, self.parts):
+            vl.vl_kl_topk_inplace(x, w.V, w.ntok, w.V, c0, width, self.tid, self.tp, w.k, w.coef, 0, w.ntok,
+                                  None, self.stats, self.labels, w.ce_coef, part, None)
+        for part in self.parts[1:]:
+            vl.vl_acc_add(self.parts[0], part, w.ntok)
+
+    def kernel(self, j):
+        """The dominant kernel: the first vocabulary slice's KL + CE pass (statistics given)."""
+        w, x = self.w, self.bufs[j]
+        c0, width = self.cuts[0]
+        self.vl.vl_kl_topk_inplace(x, w.V, w.ntok, w.V, c0, width, self.tid, self.tp, w.k, w.coef, 0, w.ntok,
+                                   None, self.stats, self.labels, w.ce_coef, self.parts[0], None)
+
+
+def nbuf_for(bytes_per_buf: int) -> int:
+    """Work buffers per round: enough that a round streams well past L2, at most 16 GB."""
+    return int(max(2, min(16, (16 << 30) // max(1, bytes_per_buf))))
+
+
+def base_workload(name):
+    return W.WORKLOADS[name.split("_k")[0] if name.startswith("topk") else name]
+
+
+def make_case(torch, name, ntok=None, nbuf=None):
+    w = base_workload(name)
+    if ntok:
+        w = w.scaled(ntok)
+    nb = nbuf or nbuf_for(w.ntok * w.V * 4)
+    if w.kind == "ce":
+        return CeFused(torch, w, nb)
+    if w.kind == "kl":
+        return Kl(torch, w, nb)
+    if w.kind == "topk":
+        k = int(name.split("_k")[1]) if "_k" in name else w.k
+        return TopK(torch, w, 1, k)
+    if w.kind == "ce_kl_sliced":
+        return LargeV(torch, w, nb)
+    raise ValueError(name)
+
+
+# ------------------------------------------------------------------ timing
+
+
+def time_case(torch, case, steps, warmup, flush, kernel_only=False):
+    """Times exactly `steps` steps; returns (total ms, per-round ms per step).
+
+    Steps run in rounds over the R work buffers.  Before a round every buffer is
+    restored from the pristine inputs and L2 is flushed (eager, untimed); the
+    round's steps are then replayed from a captured CUDA graph between two
+    events, so the device runs them back to back without waiting on the host.
+    """
+    fn = case.kernel if kernel_only else case.step
+    R = len(case.bufs)
+    for i in range(warmup):
+        j = i % R
+        case.restore(j)
+        flush()
+        fn(j)
+    torch.cuda.synchronize()
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for j in range(n):
+                    fn(j)
+            graphs[n] = g
+        return graphs[n]
+
+    per = []
+    total = 0.0
+    done = 0
+    while done < steps:
+        n = min(R, steps - done)
+        g = graph_for(n)
+        for j in range(n):
+            case.restore(j)
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        total += ms
+        per.append(ms / n)
+        done += n
+    return total, per
+
+
+def e2e_ce(torch, case, steps, warmup):
+    """The headline step through the C ABI from pinned host buffers: H2D of logits and labels,
+    vl_ce_fused, D2H of gradient, loss, lse and mean, all inside the timed region."""
+    w = case.w
+    hx = torch.from_numpy(case.x_host).pin_memory()
+    hl = torch.from_numpy(case.lab_host.view(np.int32)).pin_memory()
+    hg = torch.empty_like(hx).pin_memory()
+    hloss = torch.empty(w.ntok).pin_memory()
+    hlse = torch.empty(w.ntok).pin_memory()
+    hmean = torch.empty(1).pin_memory()
+    x, lab = case.bufs[0], case.labels
+
+    def one():
+        x.copy_(hx, non_blocking=True)
+        lab.copy_(hl, non_blocking=True)
+        case.vl.vl_ce_fused(x, w.V, w.ntok, w.V, lab, w.loss_start, w.loss_end, w.scale, case.loss, case.lse,
+                            None, case.mean, None)
+        hg.copy_(x, non_blocking=True)
+        hloss.copy_(case.loss, non_blocking=True)
+        hlse.copy_(case.lse, non_blocking=True)
+        hmean.copy_(case.mean, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # restore the pristine logits the other measurements use
+    case.bufs[0].copy_(case.pristine)
+    h2d = hx.numel() * 4 + hl.numel() * 4
+    d2h = hg.numel() * 4 + 2 * w.ntok * 4 + 4
+    return ms, h2d, d2h
+
+
+def kernel_traffic(kernel_tag: str):
+    """DRAM bytes per launch from the committed ncu summary, if the sources still match."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("csrc_sha256") != csrc_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel_tag)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "top_kl_distill_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def roofline(case, kernel_ms, peak, peak_kind, tag):
+    achieved = case.kernel_bytes() / (kernel_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+            "traffic": kernel_traffic(tag), "kernel": tag,
+            "algorithmic_bytes_per_launch": case.kernel_bytes()}
+
+
+KERNEL_TAG = {"ce_lm": "ce_fused", "ce_tiny": "ce_fused", "kl": "kl_resident", "large_v": "kl_sliced_stream"}
+
+
+def oracle_rate(name, budget_s=8.0):
+    """The CPU oracle, as it stands, on a bounded sample of the workload's rows.
+    Inputs are drawn outside the clock; only the oracle calls are timed."""
+    from oracle import vloss_oracle as O
+    w = W.WORKLOADS[name.split("_k")[0] if name.startswith("topk") else name]
+    k = int(name.split("_k")[1]) if "_k" in name else w.k
+    chunk, r, n, spent = 8, 0, 0, 0.0
+    while spent < budget_s and n < w.ntok:
+        r1 = min(w.ntok, r + chunk)
+        x = W.logits(w, r, r1, threads=1)
+        lab = W.labels(w, r, r1)
+        tid, tp = W.teacher(w, r, r1) if w.k else (None, None)
+        t0 = time.perf_counter()
+        if w.kind == "ce":
+            O.ce_fused(x, lab, 0, r1 - r, w.scale)
+        elif w.kind == "kl":
+            O.kl_topk(x, tid, tp, w.coef)
+        elif w.kind == "topk":
+            O.topk_rows(x, k)
+        else:
+            _, lse = O.ce_forward(x, lab, 0, r1 - r)
+            for c0, width in cuts_for_slices(w.V, w.slices):
+                O.kl_topk(x, tid, tp, w.coef, lse=lse, col0=c0, ncols=width, labels=lab, ce_coef=w.ce_coef)
+        spent += time.perf_counter() - t0
+        n += r1 - r
+        r = r1
+    return n / max(1e-9, spent), n, spent
+
+
+# ------------------------------------------------------------------ main
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier_max(torch, ws, value: float) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    name = args.workload
+    w = W.WORKLOADS[name]
+    from oracle import vloss_oracle as O
+    per_step_rows = 16
+    for _ in range(args.warmup):
+        x = W.logits(w, 0, per_step_rows, threads=1)
+        O.ce_fused(x, W.labels(w, 0, per_step_rows), 0, per_step_rows, w.scale)
+    total, rows = 0.0, 0
+    for s in range(args.steps):
+        r0 = (s * per_step_rows) % w.ntok
+        r1 = min(w.ntok, r0 + per_step_rows)
+        x = W.logits(w, r0, r1, threads=1)
+        lab = W.labels(w, r0, r1)
+        t0 = time.perf_counter()
+        O.ce_fused(x, lab, 0, r1 - r0, w.scale)
+        total += time.perf_counter() - t0
+        rows += r1 - r0
+    v = rows / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy)",
+        "config": {"workload": workload_desc(w), "step": f"{per_step_rows} rows of the batch per step"},
+        "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows ({per_step_rows} per step) of the {w.ntok}-row batch"},
+        "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_desc(w):
+    if w.kind == "ce":
+        return (f"{w.name}: fused CE, {w.ntok} x {w.V} fp32 logits, window [{w.loss_start}, {w.loss_end}), "
+                f"scale 1/{round(1 / w.scale)}")
+    return w.name
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="ce_lm")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=20)
+    ap.add_argument("--sweep-only", default="", help="comma-separated sweep workloads (default: all)")
+    ap.add_argument("--ntok", type=int, default=0, help="rows of a scaled-down workload (profiling only)")
+    ap.add_argument("--bufs", type=int, default=0, help="work buffers per timing round (profiling only)")
+    ap.add_argument("--no-oracle", action="store_true", help="skip the CPU baseline and the e2e leg")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(local)
+    from top_kl_distill_gb300 import vloss as vl
+    vl.lib()                                  # fails loudly if the library is not built
+    peak, peak_kind = peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    case = make_case(torch, args.workload, args.ntok or None, args.bufs or None)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    total_ms, per = time_case(torch, case, args.steps, args.warmup, flush)
+    t_wall1 = time.time()
+    total_ms = barrier_max(torch, ws, total_ms)
+    k_ms_total, k_per = time_case(torch, case, args.steps, 2, flush, kernel_only=True)
+    t_wall2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall2)
+
+    ms_step = total_ms / args.steps
+    rows_all = case.rows() * ws
+    value = rows_all / (ms_step * 1e-3)
+    kernel_ms = k_ms_total / args.steps
+    e2e_ms, h2d, d2h = (None, 0, 0)
+    if isinstance(case, CeFused) and not args.no_oracle:
+        e2e_ms, h2d, d2h = e2e_ce(torch, case, max(10, args.steps // 4), 3)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy, uploaded once)",
+        "config": {"workload": workload_desc(case.w), "ntok": case.w.ntok, "V": case.w.V,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "fresh input copy per step; a 512 MB write flushes L2 before each group of timed steps",
+                   "work_buffers": len(case.bufs)},
+        "hbm_gbs_step": round(case.bytes_per_step() / (ms_step * 1e-3) / 1e9, 1),
+        "roofline": roofline(case, kernel_ms, peak, peak_kind, KERNEL_TAG.get(case.w.name, case.w.name)),
+        "clocks": clocks,
+        "gpu_launches": case.launches_per_step * args.steps,
+    }
+    if e2e_ms is not None:
+        line["e2e"] = {"value": round(case.rows() * ws / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    if rank == 0 and not args.no_oracle:
+        rate, nrows, secs = oracle_rate(args.workload)
+        line["cpu_baseline"] = {"value": round(rate, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{nrows} of {case.w.ntok} rows, {secs:.1f} s of float64 numpy "
+                                          f"on one host core (input generation excluded)"}
+    del case
+    torch.cuda.empty_cache()
+
+    if not args.no_sweep:
+        sweep = {}
+        names = ["kl", "topk_k256", "topk_k2048", "large_v"]
+        if args.sweep_only:
+            names = [n for n in args.sweep_only.split(",") if n]
+        for name in names:
+            c = make_case(torch, name, args.ntok or None, args.bufs or None)
+            steps = args.sweep_steps
+            tot, _ = time_case(torch, c, steps, 3, flush)
+            ktot, _ = time_case(torch, c, steps, 2, flush, kernel_only=True)
+            ms = barrier_max(torch, ws, tot) / steps
+            entry = {
+                "rows_per_s": round(c.rows() * ws / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+                "hbm_gbs_step": round(c.bytes_per_step() / (ms * 1e-3) / 1e9, 1),
+                "algorithmic_bytes_per_step": c.bytes_per_step(), "steps": steps,
+                "roofline": roofline(c, ktot / steps, peak, peak_kind, KERNEL_TAG.get(c.name, c.name)),
+                "gpu_launches": c.launches_per_step * steps,
+            }
+            if rank == 0 and not args.no_oracle:
+                rate, nrows, secs = oracle_rate(name, budget_s=4.0)
+                entry["oracle_rows_per_s"] = round(rate, 2)
+            sweep[name] = entry
+            del c
+            torch.cuda.empty_cache()
+        line["sweep"] = sweep
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

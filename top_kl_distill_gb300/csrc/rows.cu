@@ -2,7 +2,7 @@
 // fp32 vocabulary logits, one persistent CTA (or cluster of CTAs) per SM.
 //
 // Layout of one launch
-//   * grid = nclusters * csize CTAs, at most one CTA per SM (the ring below takes
+//   * grid = nclusters * csize CTAs, one CTA per SM (the ring below takes
 //     ~200 KB of shared memory).  Cluster i handles rows i, i + nclusters, ...
 //   * a row slice of ncols floats is cut into a <=3-float head, a 16-byte-aligned
 //     body and a <=3-float tail.  The body is split evenly (in float4 units)
@@ -10,17 +10,24 @@
 //     the last rank the tail.
 //   * warp 0 (one lane) is the producer: it streams each CTA's body through a
 //     ring of kSlots tiles of kTileF floats with 1-D bulk copies (TMA) signalled
-//     on per-slot mbarriers; warps 1..16 are consumers.
+//     on per-slot mbarriers; warps 1..15 are consumers.  A consumer thread owns
+//     float4 number `ct` of every tile.
 //
 // Modes
-//   resident  (CE fused, KL without given statistics): the whole body part of a
-//             row sits in the ring.  Consumers reduce (max, sum exp) over it,
-//             merge across warps (shared memory) and across the cluster
-//             (distributed shared memory + remote mbarrier arrive), then emit
-//             the gradient from the staged tiles.  One HBM read, one HBM write.
-//   streaming (CE backward, KL with given statistics): each tile is turned into
-//             gradient as soon as it lands and its slot is released.
-//   reduce    (CE forward): statistics only, tiles released after reduction.
+//   self-contained (CE fused, KL without given statistics): the producer streams
+//             each row part twice.  Pass A reduces (max, sum of exponentials)
+//             online per thread; partials are merged across warps (shared
+//             memory) and across the cluster (distributed shared memory: st.async
+//             that completes the peer's mbarrier transaction count).  Pass B
+//             re-reads the part -- it was read microseconds earlier, so the bytes
+//             come from L2 -- and writes the gradient tile by tile.  HBM sees one
+//             read and one write per element; no row has to fit on chip.
+//   streaming (CE backward, KL with given statistics): pass B only.
+//   reduce    (CE forward): pass A only.
+//
+// Sparse columns (the label, the teacher's top-k ids) are fixed up after the bulk
+// store of the row and a barrier: their values are gathered from the staged tiles
+// as they pass, their gradient is rewritten, and their loss terms are reduced.
 //
 // Sources: aprender-train wgpu_cross_entropy.rs (module doc, forward_async,
 // backward: loss = lse - s[label], gradient scale * (softmax - onehot), loss
@@ -36,13 +43,18 @@
 namespace vl {
 namespace {
 
-constexpr int NCW = 16;                 // consumer warps
+constexpr int NCW = kConsumerWarps;     // consumer warps
 constexpr int NCT = NCW * 32;           // consumer threads
 constexpr int NTHREADS = NCT + 32;      // + the producer warp
-constexpr int KMAX = 1024;              // teacher support per row
+constexpr int EPT = 3;                  // teacher support entries per consumer thread
+constexpr int KMAX = EPT * NCT;         // teacher support per row
+constexpr int LT = NCT - 1;             // the consumer thread that handles the label
+constexpr int BMPW = 1024;              // words of the self-contained support bitmap
+constexpr int KSELF = 1024;             // teacher support per row, self-contained mode
 constexpr uint32_t kBarConsumers = 1;   // named barrier id used by consumers only
 
 static_assert(kTileF / 4 == NCT, "one float4 of each tile per consumer thread");
+static_assert(KMAX >= 1024, "the C ABI promises k <= 1024");
 
 __device__ unsigned int g_watchdog;
 
@@ -56,35 +68,46 @@ struct alignas(128) Smem {
     float lbuf[2][kMaxCluster];
     float2 wred[2][NCW];
     float wloss[2][NCW];
-    unsigned long long skey[KMAX];      // (column << 32 | q) of the teacher support, unsorted
-    float sp_raw[KMAX];
-    uint32_t scol[KMAX];                // support sorted by (column, q)
-    float sp[KMAX];
+    union {
+        struct {                        // streaming mode: support of the current row
+            alignas(16) int kcol[2][KMAX];   // column (slice-relative) per entry, -1 outside this CTA
+            float kp[2][KMAX];               // probability per entry
+            float ks[2][KMAX];               // the logit at that column, gathered as its tile passes
+        };
+        struct {                        // self-contained mode: three rows in flight
+            uint32_t bmp[3][BMPW];           // one bit per float4 group that holds a support id
+            int ecol[3][KSELF];              // support column (slice-relative; -1 elsewhere)
+            float ep[3][KSELF];
+            float wl3[3][NCW];               // KL loss per warp, reduced one row later
+        };
+    };
     int abort;
     uint32_t issued;
 };
 
+static_assert(sizeof(Smem) <= 227 * 1024, "shared memory of one CTA");
+
 // Columns of one row slice handled by CTA `rank` of `c` (relative to the slice start).
 struct Part {
-    long long h;    // head length (first columns up to the 16-byte boundary)
-    long long hn;   // head columns this CTA handles
-    long long b0;   // first body column of this CTA
-    long long bn;   // body columns of this CTA (a multiple of 4)
-    long long t0;   // first tail column
-    long long tn;   // tail columns this CTA handles
-    long long lo;   // this CTA owns columns [lo, hi)
-    long long hi;
+    int h;     // head length (first columns up to the 16-byte boundary)
+    int hn;    // head columns this CTA handles
+    int b0;    // first body column of this CTA
+    int bn;    // body columns of this CTA (a multiple of 4)
+    int t0;    // first tail column
+    int tn;    // tail columns this CTA handles
+    int lo;    // this CTA owns columns [lo, hi)
+    int hi;
 };
 
-__device__ __forceinline__ Part part_of(const float* rowp, long long n, int rank, int c) {
+__device__ __forceinline__ Part part_of(const float* rowp, int n, int rank, int c) {
     Part p;
-    const long long mis = (long long)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
-    long long h = (4 - mis) & 3;
+    const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
+    int h = (4 - mis) & 3;
     if (h > n) h = n;
-    const long long bt = (n - h) & ~3LL;
-    const long long per = (((bt >> 2) + c - 1) / c) * 4;
-    const long long s = min((long long)rank * per, bt);
-    const long long e = min((long long)(rank + 1) * per, bt);
+    const int bt = (n - h) & ~3;
+    const int per = (((bt >> 2) + c - 1) / c) * 4;
+    const int s = min(rank * per, bt);
+    const int e = min((rank + 1) * per, bt);
     p.h = h;
     p.hn = rank == 0 ? h : 0;
     p.b0 = h + s;
@@ -102,43 +125,53 @@ __device__ __forceinline__ bool row_loaded(const RowParams& P, long long r) {
     return r >= P.ls && r < P.le;
 }
 
-__device__ __forceinline__ float pick(const float4& v, long long d) {
-    return d == 0 ? v.x : d == 1 ? v.y : d == 2 ? v.z : v.w;
+// softmax value from the row statistics: exp((s - m) - lnS)
+__device__ __forceinline__ float soft(float s, float m, float lnS) {
+    return ex2(((s - m) - lnS) * kLog2e);
 }
 
-__device__ __forceinline__ void sub_at(float4& o, long long d, float a) {
+__device__ __forceinline__ void sub_at(float4& o, unsigned d, float a) {
     if (d == 0) o.x -= a;
     else if (d == 1) o.y -= a;
     else if (d == 2) o.z -= a;
     else o.w -= a;
 }
 
-// softmax value from the row statistics: exp((s - m) - lnS)
-__device__ __forceinline__ float soft(float s, float m, float lnS) {
-    return ex2(((s - m) - lnS) * kLog2e);
-}
+__device__ __forceinline__ float max4(const float4& v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
 
 // ---------------------------------------------------------------- producer
 
-template <int OP>
+// Issue the body tiles of one row part; false if a wait gave up.
+__device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long long r, int rank, uint32_t& g) {
+    const float* rowp = P.x + r * P.ld + P.col0;
+    const Part pt = part_of(rowp, (int)P.ncols, rank, P.csize);
+    for (int c0 = 0; c0 < pt.bn; c0 += kTileF) {
+        const uint32_t slot = g % kSlots, use = g / kSlots;
+        if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog)) return false;
+        const uint32_t bytes = (uint32_t)min(kTileF, pt.bn - c0) * 4u;
+        mbar_arrive_expect_tx(&S.full[slot], bytes);
+        bulk_g2s(S.ring[slot], rowp + pt.b0 + c0, bytes, &S.full[slot]);
+        ++g;
+    }
+    return true;
+}
+
+// Tile order: one pass per row for the streaming and reduce modes; for the
+// self-contained mode pass A of a row, then pass B of the row before it, so the
+// reads of the next row are in flight while the current one is written.
+template <int OP, bool RES>
 __device__ void producer(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     uint32_t g = 0;
+    long long prev = -1;
     for (long long r = cid; r < P.ntok; r += ncl) {
         if (!row_loaded<OP>(P, r)) continue;
-        const float* rowp = P.x + r * P.ld + P.col0;
-        const Part pt = part_of(rowp, P.ncols, rank, P.csize);
-        for (long long c0 = 0; c0 < pt.bn; c0 += kTileF) {
-            const uint32_t slot = g % kSlots, use = g / kSlots;
-            if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog)) {
-                S.issued = g;
-                return;
-            }
-            const uint32_t bytes = (uint32_t)min((long long)kTileF, pt.bn - c0) * 4u;
-            mbar_arrive_expect_tx(&S.full[slot], bytes);
-            bulk_g2s(S.ring[slot], rowp + pt.b0 + c0, bytes, &S.full[slot]);
-            ++g;
+        if (!issue_part(P, S, r, rank, g)) break;
+        if (RES) {
+            if (prev >= 0 && !issue_part(P, S, prev, rank, g)) break;
+            prev = r;
         }
     }
+    if (RES && prev >= 0 && !S.abort) issue_part(P, S, prev, rank, g);
     S.issued = g;
 }
 
@@ -153,62 +186,46 @@ __device__ void drain(Smem& S) {
 
 __device__ void zero_part(float* rowp, const Part& pt, int ct) {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long long i = ct; i < (pt.bn >> 2); i += NCT) st_global_v4(rowp + pt.b0 + 4 * i, z);
+    for (int i = ct; i < (pt.bn >> 2); i += NCT) st_global_v4(rowp + pt.b0 + 4 * i, z);
     if (ct < pt.hn) rowp[ct] = 0.f;
     if (ct >= 4 && ct - 4 < pt.tn) rowp[pt.t0 + ct - 4] = 0.f;
 }
 
-// Teacher support of row r inside this CTA's columns, sorted by (column, q) into
-// S.scol / S.sp.  Returns the number of entries.  Ids >= V are counted as errors.
-__device__ int load_support(const RowParams& P, Smem& S, long long r, const Part& pt, int rank, int ct) {
-    const int k = P.k;
-    bool in[2] = {false, false};
-    unsigned long long key[2] = {~0ull, ~0ull};
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-        const int q = ct + rep * NCT;
-        if (q < k) {
-            const uint32_t id = P.tid[r * k + q];
-            const float p = P.tp[r * k + q];
-            if ((long long)id >= P.V) {
-                if (rank == 0 && P.err) atomicAdd(P.err, 1);
-            } else {
-                const long long rel = (long long)id - P.col0;
-                if (rel >= pt.lo && rel < pt.hi) key[rep] = ((unsigned long long)rel << 32) | (unsigned)q;
-            }
-            S.skey[q] = key[rep];
-            S.sp_raw[q] = p;
-            in[rep] = key[rep] != ~0ull;
-        }
+// A sparse column this thread looks after: where it sits in the row part, and its
+// logit once the tile holding it has passed.
+struct Sparse {
+    int col;     // slice-relative column, -1 if none
+    int rel;     // column - b0 inside this CTA's body (tile = rel / kTileF), -1 for head/tail
+    float s;     // the logit
+};
+
+__device__ __forceinline__ void locate(Sparse& e, const Part& pt, const float* rowp) {
+    if (e.col >= pt.b0 && e.col < pt.b0 + pt.bn) {
+        e.rel = e.col - pt.b0;
+    } else {
+        e.rel = -1;
+        e.s = rowp[e.col];     // head or tail: read before anything of the row is written
     }
-    uint32_t n = named_sync_popc(kBarConsumers, NCT, in[0]);
-    if (k > NCT) n += named_sync_popc(kBarConsumers, NCT, in[1]);
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-        const int q = ct + rep * NCT;
-        if (q < k && in[rep]) {
-            int pos = 0;
-            for (int j = 0; j < k; ++j) pos += S.skey[j] < key[rep] ? 1 : 0;
-            S.scol[pos] = (uint32_t)(key[rep] >> 32);
-            S.sp[pos] = S.sp_raw[q];
-        }
-    }
-    named_sync(kBarConsumers, NCT);
-    return (int)n;
 }
 
-// KL terms of the support entries [e0, e1) that fall on columns [c0, c0 + 4):
-// subtract coef * p from the gradient and add p (ln p - (s - lse)) to the loss.
-__device__ __forceinline__ void kl_apply4(const Smem& S, uint32_t e0, uint32_t e1, long long c0, const float4& v,
-                                          float4& o, float coef, float m, float lnS, float& lacc) {
-    for (uint32_t e = e0; e < e1; ++e) {
-        const long long d = (long long)S.scol[e] - c0;
-        if (d >= 0 && d < 4) {
-            const float p = S.sp[e];
-            sub_at(o, d, coef * p);
-            if (p > 0.f) lacc += p * (logf(p) - ((pick(v, d) - m) - lnS));
-        }
-    }
+__device__ __forceinline__ void gather(Sparse& e, int t, const float* tile) {
+    if (e.rel >= 0 && (e.rel / kTileF) == t) e.s = tile[e.rel % kTileF];
+}
+
+__device__ __forceinline__ void gather_support(Smem& S, uint32_t kb, const int (&erel)[EPT], int ct, int t,
+                                               const float* tile) {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i)
+        if (erel[i] >= 0 && erel[i] / kTileF == t) S.ks[kb][ct + i * NCT] = tile[erel[i] % kTileF];
+}
+
+// (max, sum) of n partials: the max first, then the sums rescaled independently.
+__device__ __forceinline__ MaxSum combine(const float2* part, int n) {
+    float M = part[0].x;
+    for (int i = 1; i < n; ++i) M = fmaxf(M, part[i].x);
+    float T = 0.f;
+    for (int i = 0; i < n; ++i) T += part[i].y * ex2((part[i].x - M) * kLog2e);
+    return MaxSum{M, T};
 }
 
 // ---------------------------------------------------------------- consumer
@@ -219,181 +236,215 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
     const int c = P.csize;
-    uint32_t g = 0, nred = 0, nloss = 0, nx = 0, nlx = 0;
+    const int ncols = (int)P.ncols;
+    uint32_t g = 0, nred = 0, nloss = 0, nx = 0, nlx = 0, nrow = 0;
     const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
+    const float cg = P.cg;
+    // the label and support entry q = ct of the next row, loaded one row ahead
+    uint32_t nlab = 0, nid = 0;
+    float np = 0.f;
+    auto prefetch = [&](long long rr) {
+        if (rr >= P.ntok) return;
+        if (has_label) nlab = P.labels[rr];
+        if (kKL && ct < P.k) { nid = P.tid[rr * P.k + ct]; np = P.tp[rr * P.k + ct]; }
+    };
+    prefetch(cid);
 
     for (long long r = cid; r < P.ntok; r += ncl) {
+        const uint32_t lab_r = nlab, id0 = nid;
+        const float p0 = np;
+        prefetch(r + ncl);
         float* rowp = P.x + r * P.ld + P.col0;
-        const Part pt = part_of(rowp, P.ncols, rank, c);
+        const Part pt = part_of(rowp, ncols, rank, c);
         const bool inwin = r >= P.ls && r < P.le;
-        const uint32_t nt = (uint32_t)((pt.bn + kTileF - 1) / kTileF);
-        if (RES && nt > (uint32_t)kSlots && ct == 0) {
-            // the host never launches this; unwind rather than wait on a ring that cannot fill
-            S.abort = 1;
-            atomicOr(&g_watchdog, 2u);
-        }
-
+        const int nt = (pt.bn + kTileF - 1) / kTileF;
         if (!row_loaded<OP>(P, r)) {
             zero_part(rowp, pt, ct);
             if (ct == 0 && rank == 0 && P.loss) P.loss[r] = 0.f;
             continue;
         }
+        const uint32_t kb = nrow & 1u;
+        ++nrow;
 
-        // the label as a slice-relative column; -1 when there is none
-        long long jl = -1;
+        // ---- the label: its slice column jl (every thread), its logit (thread LT);
+        //      the teacher support: entry q on thread q % NCT
+        int jl = -1;
         bool bad_label = false;
         if (has_label) {
-            const uint32_t lab = P.labels[r];
-            if ((long long)lab >= P.V) bad_label = true;
-            else jl = (long long)lab - P.col0;
+            const uint32_t l = lab_r;
+            if ((long long)l >= P.V) bad_label = true;
+            else if ((long long)l >= P.col0 && (long long)l < P.col0 + ncols) jl = (int)((long long)l - P.col0);
         }
-        if (bad_label && inwin && rank == 0 && ct == 0 && P.err) atomicAdd(P.err, 1);
-
-        int nsup = 0;
-        if (kKL && inwin) nsup = load_support(P, S, r, pt, rank, ct);
-
-        float m, lnS;
-        float hv = 0.f, tv = 0.f;
-        float s_label = 0.f;
-        bool own_label = false;
-        const bool has_head = ct < pt.hn;
-        const bool has_tail = ct >= 4 && ct - 4 < pt.tn;
-
-        if (RES || OP == kCeFwd) {
-            // ---- statistics of the row: (max, sum exp) over head, body tiles and tail
-            MaxSum ms = ms_empty();
-            if (has_head) { hv = rowp[ct]; ms_add(ms, hv); }
-            if (has_tail) { tv = rowp[pt.t0 + ct - 4]; ms_add(ms, tv); }
-            for (uint32_t t = 0; t < nt; ++t) {
-                const uint32_t gt = g + t, slot = gt % kSlots;
-                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
-                const long long tc0 = pt.b0 + (long long)t * kTileF;
-                const int n4 = (int)(min((long long)kTileF, pt.bn - (long long)t * kTileF) >> 2);
-                if (ct < n4) {
-                    const float4 v = ld_shared_v4(&S.ring[slot][ct * 4]);
-                    ms_add4(ms, v);
-                    if (OP == kCeFwd) {
-                        const long long d = jl - (tc0 + 4 * ct);
-                        if (d >= 0 && d < 4) { own_label = true; s_label = pick(v, d); }
+        if (bad_label && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
+        Sparse lab{-1, -1, 0.f};
+        if (ct == LT && jl >= pt.lo && jl < pt.hi) { lab.col = jl; locate(lab, pt, rowp); }
+        // support entry q = ct + i * NCT: its body offset in erel[i] (-1: head/tail or none)
+        int erel[EPT] = {-1, -1, -1};
+        if (kKL && inwin) {
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int q = ct + i * NCT;
+                if (q < P.k) {
+                    const uint32_t id = i == 0 ? id0 : P.tid[r * P.k + q];
+                    int col = -1;
+                    if ((long long)id >= P.V) {
+                        if (rank == 0 && P.err) atomicAdd(P.err, 1);
+                    } else {
+                        const long long j = (long long)id - P.col0;
+                        if (j >= pt.lo && j < pt.hi) col = (int)j;
+                    }
+                    S.kcol[kb][q] = col;
+                    S.kp[kb][q] = i == 0 ? p0 : P.tp[r * P.k + q];
+                    if (col >= 0) {
+                        if (col >= pt.b0 && col < pt.b0 + pt.bn) erel[i] = col - pt.b0;
+                        else S.ks[kb][q] = rowp[col];    // head or tail: before anything is written
                     }
                 }
-                if (OP == kCeFwd) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&S.empty[slot]);
-                }
             }
-            if (OP == kCeFwd) {
-                g += nt;
-                if (has_head && jl == ct) { own_label = true; s_label = hv; }
-                if (has_tail && jl == pt.t0 + ct - 4) { own_label = true; s_label = tv; }
+        }
+
+        // head and tail columns: one per thread, finished after the sparse barrier
+        const bool has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
+        const int jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
+        const float ht = has_ht ? rowp[jht] : 0.f;
+        float m, lnS;
+
+        if (OP == kCeFwd || RES) {
+            // ---- pass A: (max, sum) online over the streamed tiles; sparse logits gathered
+            MaxSum ms = ms_empty();
+            if (has_ht) ms_add(ms, ht);
+            for (int t = 0; t < nt; ++t) {
+                const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
+                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+                const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+                if (ct < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][ct * 4]));
+                if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
+                if (ct == LT) gather(lab, t, S.ring[slot]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
+            g += (uint32_t)nt;
             ms = ms_warp_reduce(ms);
             const uint32_t b = nred & 1u;
             ++nred;
             if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
             named_sync(kBarConsumers, NCT);
-            MaxSum tot{S.wred[b][0].x, S.wred[b][0].y};
-#pragma unroll
-            for (int w = 1; w < NCW; ++w) tot = ms_merge(tot, MaxSum{S.wred[b][w].x, S.wred[b][w].y});
-            if (c > 1) {
+            MaxSum tot = combine(S.wred[b], NCW);
+            if (RES && c > 1) {
                 const uint32_t xb = nx & 1u, xpar = (nx >> 1) & 1u;
                 ++nx;
                 if (ct == 0) {
-                    for (int q = 0; q < c; ++q) {
-                        st_cluster_f32x2(map_to_rank(&S.xbuf[xb][rank], (uint32_t)q), tot.m, tot.s);
-                        mbar_arrive_remote_release(map_to_rank(&S.xbar[xb], (uint32_t)q));
-                    }
+                    mbar_arrive_expect_tx(&S.xbar[xb], 8u * (uint32_t)c);
+                    for (int q = 0; q < c; ++q)
+                        st_async_f32x2(map_to_rank(&S.xbuf[xb][rank], (uint32_t)q), tot.m, tot.s,
+                                       map_to_rank(&S.xbar[xb], (uint32_t)q));
                 }
                 wait_parity<true>(&S.xbar[xb], xpar, &S.abort, &g_watchdog);
-                tot = MaxSum{S.xbuf[xb][0].x, S.xbuf[xb][0].y};
-                for (int q = 1; q < c; ++q) tot = ms_merge(tot, MaxSum{S.xbuf[xb][q].x, S.xbuf[xb][q].y});
+                tot = combine(S.xbuf[xb], c);
             }
             m = tot.m;
             lnS = logf(tot.s);
-            if (rank == 0 && ct == 0) {
+            if (rank == 0 && ct == LT) {
                 if (P.lse_out) P.lse_out[r] = m + lnS;
                 if (P.stats_out) { P.stats_out[2 * r] = m; P.stats_out[2 * r + 1] = lnS; }
+            }
+            if (OP == kCeFwd) {
+                if (ct == LT) {
+                    if (!inwin) P.loss[r] = 0.f;
+                    else if (bad_label) P.loss[r] = __int_as_float(0x7fc00000);
+                    else if (lab.col >= 0) P.loss[r] = (m - lab.s) + lnS;
+                }
+                continue;
             }
         } else {
             if (P.stats_in) { m = P.stats_in[2 * r]; lnS = P.stats_in[2 * r + 1]; }
             else { m = P.lse_in[r]; lnS = 0.f; }
         }
 
-        if (OP == kCeFwd) {
-            if (inwin && own_label) P.loss[r] = (m - s_label) + lnS;
-            if (rank == 0 && ct == 0) {
-                if (!inwin) P.loss[r] = 0.f;
-                else if (bad_label) P.loss[r] = __int_as_float(0x7fc00000);
-            }
-            continue;
-        }
-
-        // ---- gradient, written in place from the staged tiles
-        const float cg = P.cg;
-        float lacc = 0.f;
-        uint32_t e_lo = 0;
-        if (kKL) while (e_lo < (uint32_t)nsup && (long long)S.scol[e_lo] < pt.b0) ++e_lo;
-        for (uint32_t t = 0; t < nt; ++t) {
-            const uint32_t gt = g + t, slot = gt % kSlots;
-            if (!RES) wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
-            const long long tc0 = pt.b0 + (long long)t * kTileF;
-            const long long n = min((long long)kTileF, pt.bn - (long long)t * kTileF);
-            uint32_t e_hi = e_lo;
-            if (kKL) while (e_hi < (uint32_t)nsup && (long long)S.scol[e_hi] < tc0 + n) ++e_hi;
-            if (ct < (int)(n >> 2)) {
-                const long long c0 = tc0 + 4 * ct;
-                const float4 v = ld_shared_v4(&S.ring[slot][ct * 4]);
-                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (inwin) {
-                    o.x = cg * soft(v.x, m, lnS);
-                    o.y = cg * soft(v.y, m, lnS);
-                    o.z = cg * soft(v.z, m, lnS);
-                    o.w = cg * soft(v.w, m, lnS);
-                    const long long d = jl - c0;
-                    if (d >= 0 && d < 4) {
-                        sub_at(o, d, P.ce_coef);
-                        own_label = true;
-                        s_label = pick(v, d);
-                    }
-                    if (kKL && e_hi > e_lo) kl_apply4(S, e_lo, e_hi, c0, v, o, P.coef, m, lnS, lacc);
+        // ---- pass B: each tile turned into gradient as it lands (zeros outside the window)
+        {
+            const float c1 = inwin ? cg : 0.f;
+            for (int t = 0; t < nt; ++t) {
+                const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
+                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+                const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+                if (ct < n4) {
+                    const float4 x = ld_shared_v4(&S.ring[slot][ct * 4]);
+                    const float4 o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
+                                                 c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
+                    st_global_v4(rowp + pt.b0 + t * kTileF + 4 * ct, o);
                 }
-                st_global_v4(rowp + c0, o);
+                if (!RES) {
+                    if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
+                    if (ct == LT) gather(lab, t, S.ring[slot]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty[slot]);
-            e_lo = e_hi;
+            g += (uint32_t)nt;
         }
-        g += nt;
 
-        // head and tail elements (scalar)
-        if (has_head || has_tail) {
-            const long long j = has_head ? (long long)ct : pt.t0 + ct - 4;
-            const float s = has_head ? (RES ? hv : rowp[j]) : (RES ? tv : rowp[j]);
+        // ---- sparse columns, once every bulk store of the row is done: the label,
+        //      the support ids, and the head/tail columns with their corrections
+        named_sync(kBarConsumers, NCT);
+        float lacc = 0.f;
+        if (has_ht) {
             float o = 0.f;
             if (inwin) {
-                o = cg * soft(s, m, lnS);
-                if (j == jl) { o -= P.ce_coef; own_label = true; s_label = s; }
-                if (kKL) {
-                    for (uint32_t e = 0; e < (uint32_t)nsup; ++e) {
-                        if ((long long)S.scol[e] == j) {
-                            const float p = S.sp[e];
-                            o -= P.coef * p;
-                            if (p > 0.f) lacc += p * (logf(p) - ((s - m) - lnS));
-                        }
+                o = cg * soft(ht, m, lnS);
+                if (kKL)
+                    for (int j = 0; j < P.k; ++j)
+                        if (S.kcol[kb][j] == jht) o -= P.coef * S.kp[kb][j];
+                if (jht == jl) o -= P.ce_coef;
+            }
+            rowp[jht] = o;
+        }
+        if (inwin) {
+            if (kKL) {
+#pragma unroll
+                for (int i = 0; i < EPT; ++i) {
+                    const int q = ct + i * NCT;
+                    if (q >= P.k) continue;
+                    const int col = S.kcol[kb][q];
+                    if (col < 0) continue;
+                    const float pq = S.kp[kb][q], sq = S.ks[kb][q];
+                    if (pq > 0.f) lacc += pq * (logf(pq) - ((sq - m) - lnS));
+                    if (erel[i] < 0) continue;         // head/tail columns: finished above
+                    // repeated ids: the lowest q writes the column, with every entry's p
+                    bool first = true;
+                    float psum = 0.f;
+                    const int4* kc4 = reinterpret_cast<const int4*>(S.kcol[kb]);
+                    for (int j4 = 0; j4 < (P.k + 3) >> 2; ++j4) {
+                        const int4 cc = kc4[j4];
+                        const int j = 4 * j4;
+                        if (cc.x == col && j < P.k) { first &= j >= q; psum += S.kp[kb][j]; }
+                        if (cc.y == col && j + 1 < P.k) { first &= j + 1 >= q; psum += S.kp[kb][j + 1]; }
+                        if (cc.z == col && j + 2 < P.k) { first &= j + 2 >= q; psum += S.kp[kb][j + 2]; }
+                        if (cc.w == col && j + 3 < P.k) { first &= j + 3 >= q; psum += S.kp[kb][j + 3]; }
+                    }
+                    if (first) {
+                        float o = cg * soft(sq, m, lnS) - P.coef * psum;
+                        if (col == jl) o -= P.ce_coef;
+                        rowp[col] = o;
                     }
                 }
             }
-            rowp[j] = o;
+            if (ct == LT && lab.col >= 0 && lab.rel >= 0) {
+                bool in_support = false;
+                if (kKL)
+                    for (int j = 0; j < P.k; ++j) in_support |= S.kcol[kb][j] == lab.col;
+                if (!in_support) rowp[lab.col] = cg * soft(lab.s, m, lnS) - P.ce_coef;
+            }
         }
 
         // ---- losses
         if (OP == kCeFused || OP == kCeBwd) {
             if (P.loss) {
-                if (inwin && own_label) P.loss[r] = (m - s_label) + lnS;
-                if (rank == 0 && ct == 0) {
+                if (ct == LT && inwin && lab.col >= 0) P.loss[r] = (m - lab.s) + lnS;
+                if (rank == 0 && ct == LT) {
                     if (!inwin) P.loss[r] = 0.f;
                     else if (bad_label) P.loss[r] = __int_as_float(0x7fc00000);
-                    else if (jl < 0 || jl >= P.ncols) P.loss[r] = 0.f;   // label in another slice
+                    else if (jl < 0) P.loss[r] = 0.f;   // the label lies in another slice
                 }
             }
         } else if (kKL) {
@@ -410,8 +461,8 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 } else {
                     const uint32_t lb = nlx & 1u, lpar = (nlx >> 1) & 1u;
                     ++nlx;
-                    st_cluster_f32(map_to_rank(&S.lbuf[lb][rank], 0u), L);
-                    mbar_arrive_remote_release(map_to_rank(&S.lbar[lb], 0u));
+                    if (rank == 0) mbar_arrive_expect_tx(&S.lbar[lb], 4u * (uint32_t)c);
+                    st_async_f32(map_to_rank(&S.lbuf[lb][rank], 0u), L, map_to_rank(&S.lbar[lb], 0u));
                     if (rank == 0) {
                         wait_parity<true>(&S.lbar[lb], lpar, &S.abort, &g_watchdog);
                         float T = 0.f;
@@ -419,6 +470,283 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                         P.loss[r] = T;
                     }
                 }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- self-contained consumer
+
+// Pass B of a row whose statistics are known: the gradient tile by tile, the label
+// and the teacher support corrected inline, the KL loss terms accumulated.
+struct Pending {
+    long long r;
+    float* rowp;
+    Part pt;
+    int nt;
+    bool inwin, bad;
+    int jl;          // slice-relative label column, -1 when none or outside this CTA's columns
+    float m, lnS;
+    uint32_t b3;     // buffer of its support, bitmap and KL loss
+    bool has_ht;
+    int jht;
+    float ht;
+};
+
+template <int OP>
+__device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
+                                        int rank, int gs) {
+    constexpr bool kKL = OP == kKl;
+    const float c1 = w.inwin ? P.cg : 0.f;
+    float lacc = 0.f;
+    for (int t = 0; t < w.nt; ++t) {
+        const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
+        wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+        const int n4 = min(kTileF, w.pt.bn - t * kTileF) >> 2;
+        const int c0 = w.pt.b0 + t * kTileF + 4 * ct;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), o = x;
+        uint32_t hit = 0u;
+        if (ct < n4) {
+            x = ld_shared_v4(&S.ring[slot][ct * 4]);
+            o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS), c1 * soft(x.z, w.m, w.lnS),
+                            c1 * soft(x.w, w.m, w.lnS));
+            if (w.inwin) {
+                const unsigned d = (unsigned)(w.jl - c0);
+                if (d < 4u) {
+                    const float xs = d == 0 ? x.x : d == 1 ? x.y : d == 2 ? x.z : x.w;
+                    sub_at(o, d, P.ce_coef);
+                    if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
+                }
+            }
+            if (kKL && w.inwin) {
+                const uint32_t bi = (uint32_t)(t * NCT + ct) >> gs;
+                hit = (S.bmp[w.b3][bi >> 5] >> (bi & 31u)) & 1u;
+            }
+        }
+        if (kKL && w.inwin) {
+            // a flagged float4 holds a support id: the whole warp walks the support list
+            uint32_t hits = __ballot_sync(0xffffffffu, hit != 0u);
+            while (hits) {
+                const int src = __ffs(hits) - 1;
+                hits &= hits - 1u;
+                const int cs = __shfl_sync(0xffffffffu, c0, src);
+                const float x0 = __shfl_sync(0xffffffffu, x.x, src), x1 = __shfl_sync(0xffffffffu, x.y, src);
+                const float x2 = __shfl_sync(0xffffffffu, x.z, src), x3 = __shfl_sync(0xffffffffu, x.w, src);
+                float4 corr = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j0 = 0; j0 < P.k; j0 += 32) {
+                    const int j = j0 + lane;
+                    const unsigned de = j < P.k ? (unsigned)(S.ecol[w.b3][j] - cs) : 4u;
+                    if (de < 4u) {
+                        const float p = S.ep[w.b3][j];
+                        const float xs = de == 0 ? x0 : de == 1 ? x1 : de == 2 ? x2 : x3;
+                        sub_at(corr, de, -P.coef * p);
+                        if (p > 0.f) lacc += p * (logf(p) - ((xs - w.m) - w.lnS));
+                    }
+                }
+                corr.x = warp_sum(corr.x);
+                corr.y = warp_sum(corr.y);
+                corr.z = warp_sum(corr.z);
+                corr.w = warp_sum(corr.w);
+                if (lane == src) { o.x -= corr.x; o.y -= corr.y; o.z -= corr.z; o.w -= corr.w; }
+            }
+        }
+        if (ct < n4) st_global_v4(w.rowp + c0, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+    }
+    g += (uint32_t)w.nt;
+    if (w.has_ht) {
+        float o = c1 * soft(w.ht, w.m, w.lnS);
+        if (w.inwin) {
+            if (w.jht == w.jl) {
+                o -= P.ce_coef;
+                if (OP == kCeFused) P.loss[w.r] = (w.m - w.ht) + w.lnS;
+            }
+            if (kKL)
+                for (int e = 0; e < P.k; ++e)
+                    if (S.ecol[w.b3][e] == w.jht) {
+                        const float p = S.ep[w.b3][e];
+                        o -= P.coef * p;
+                        if (p > 0.f) lacc += p * (logf(p) - ((w.ht - w.m) - w.lnS));
+                    }
+        }
+        w.rowp[w.jht] = o;
+    }
+    if (OP == kCeFused && rank == 0 && ct == LT) {
+        if (!w.inwin) P.loss[w.r] = 0.f;
+        else if (w.bad) P.loss[w.r] = __int_as_float(0x7fc00000);
+    }
+    return lacc;
+}
+
+template <int OP>
+__device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
+    constexpr bool kKL = OP == kKl;
+    const int ct = (int)threadIdx.x - 32;
+    const int cw = ct >> 5, lane = ct & 31;
+    const int c = P.csize;
+    const int ncols = (int)P.ncols;
+    const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
+    // bitmap granularity: 2^gs float4 per bit, so that any row part fits BMPW words
+    int gs = 0;
+    while ((((ncols + 3) >> 2) >> gs) > BMPW * 32) ++gs;
+    uint32_t g = 0, nred = 0, nx = 0, li = 0;
+    long long rm1 = -1, rm2 = -1;      // rows of the last two passes B, for the deferred KL loss
+    if (kKL) for (int i = ct; i < BMPW; i += NCT) S.bmp[0][i] = 0u;
+    uint32_t nlab = 0, nid = 0;
+    float np = 0.f;
+    auto prefetch = [&](long long rr) {
+        if (rr >= P.ntok) return;
+        if (has_label) nlab = P.labels[rr];
+        if (kKL && ct < P.k) { nid = P.tid[rr * P.k + ct]; np = P.tp[rr * P.k + ct]; }
+    };
+    prefetch(cid);
+    Pending pend;
+    pend.r = -1;
+
+    for (long long r = cid; r < P.ntok; r += ncl) {
+        const uint32_t lab_r = nlab, id0 = nid;
+        const float p0 = np;
+        prefetch(r + ncl);
+        float* rowp = P.x + r * P.ld + P.col0;
+        const Part pt = part_of(rowp, ncols, rank, c);
+        const bool inwin = r >= P.ls && r < P.le;
+        if (!row_loaded<OP>(P, r)) {
+            zero_part(rowp, pt, ct);
+            if (ct == 0 && rank == 0) P.loss[r] = 0.f;
+            continue;
+        }
+        const uint32_t b3 = li % 3u;
+        Pending cur;
+        cur.r = r;
+        cur.rowp = rowp;
+        cur.pt = pt;
+        cur.nt = (pt.bn + kTileF - 1) / kTileF;
+        cur.inwin = inwin;
+        cur.b3 = b3;
+        cur.jl = -1;
+        cur.bad = false;
+        if (has_label) {
+            if ((long long)lab_r >= P.V) cur.bad = true;
+            else {
+                const long long j = (long long)lab_r - P.col0;
+                if (j >= pt.lo && j < pt.hi) cur.jl = (int)j;
+            }
+        }
+        if (cur.bad && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
+        if (kKL && inwin) {
+            for (int i = 0; i < EPT; ++i) {
+                const int q = ct + i * NCT;
+                if (q >= P.k) break;
+                const uint32_t id = i == 0 ? id0 : P.tid[r * P.k + q];
+                int col = -1;
+                if ((long long)id >= P.V) {
+                    if (rank == 0 && P.err) atomicAdd(P.err, 1);
+                } else {
+                    const long long j = (long long)id - P.col0;
+                    if (j >= pt.lo && j < pt.hi) col = (int)j;
+                }
+                S.ecol[b3][q] = col;
+                S.ep[b3][q] = i == 0 ? p0 : P.tp[r * P.k + q];
+            }
+        }
+        cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
+        cur.jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
+        cur.ht = cur.has_ht ? rowp[cur.jht] : 0.f;
+
+        // ---- pass A: (max, sum) online over the streamed tiles
+        MaxSum ms = ms_empty();
+        if (cur.has_ht) ms_add(ms, cur.ht);
+        for (int t = 0; t < cur.nt; ++t) {
+            const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
+            wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+            const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+            if (ct < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][ct * 4]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
+        }
+        g += (uint32_t)cur.nt;
+        ms = ms_warp_reduce(ms);
+        const uint32_t b = nred & 1u;
+        ++nred;
+        if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
+        named_sync(kBarConsumers, NCT);
+        MaxSum tot = combine(S.wred[b], NCW);
+        if (c > 1) {
+            const uint32_t xb = nx & 1u, xpar = (nx >> 1) & 1u;
+            ++nx;
+            if (ct == 0) {
+                mbar_arrive_expect_tx(&S.xbar[xb], 8u * (uint32_t)c);
+                for (int q = 0; q < c; ++q)
+                    st_async_f32x2(map_to_rank(&S.xbuf[xb][rank], (uint32_t)q), tot.m, tot.s,
+                                   map_to_rank(&S.xbar[xb], (uint32_t)q));
+            }
+            wait_parity<true>(&S.xbar[xb], xpar, &S.abort, &g_watchdog);
+            tot = combine(S.xbuf[xb], c);
+        }
+        cur.m = tot.m;
+        cur.lnS = logf(tot.s);
+        if (rank == 0 && ct == LT) {
+            if (P.lse_out) P.lse_out[r] = cur.m + cur.lnS;
+            if (P.stats_out) { P.stats_out[2 * r] = cur.m; P.stats_out[2 * r + 1] = cur.lnS; }
+        }
+        // ---- after this row's barrier: every pass B up to two rows back is done
+        if (kKL) {
+            const uint32_t nb = (li + 1u) % 3u;
+            for (int i = ct; i < BMPW; i += NCT) S.bmp[nb][i] = 0u;
+            if (inwin) {
+                for (int i = 0; i < EPT; ++i) {
+                    const int q = ct + i * NCT;
+                    if (q >= P.k) break;
+                    const int col = S.ecol[b3][q];
+                    if (col >= pt.b0 && col < pt.b0 + pt.bn) {
+                        const uint32_t bi = (uint32_t)((col - pt.b0) >> 2) >> gs;
+                        atomicOr(&S.bmp[b3][bi >> 5], 1u << (bi & 31u));
+                    }
+                }
+            }
+            if (ct == 0 && rm1 >= 0) {           // pass B of loaded row li - 2 is done
+                float L = 0.f;
+                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 1u) % 3u][w];
+                P.loss[rm1] = L;
+            }
+        }
+        // ---- pass B of the previous row
+        if (pend.r >= 0) {
+            float lacc = pass_b<OP>(P, S, pend, g, ct, lane, rank, gs);
+            if (kKL) {
+                lacc = warp_sum(lacc);
+                if (lane == 0) S.wl3[pend.b3][cw] = lacc;
+            }
+            rm2 = rm1;
+            rm1 = pend.r;
+        }
+        pend = cur;
+        ++li;
+    }
+    if (pend.r >= 0) {
+        named_sync(kBarConsumers, NCT);          // the last row's bitmap is set
+        float lacc = pass_b<OP>(P, S, pend, g, ct, lane, rank, gs);
+        if (kKL) {
+            lacc = warp_sum(lacc);
+            if (lane == 0) S.wl3[pend.b3][cw] = lacc;
+        }
+        rm2 = rm1;
+        rm1 = pend.r;
+    }
+    if (kKL) {
+        named_sync(kBarConsumers, NCT);
+        if (ct == 0) {
+            // rows li-2 and li-1 (in loaded order) still owe their loss
+            if (rm2 >= 0) {
+                float L = 0.f;
+                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 1u) % 3u][w];
+                P.loss[rm2] = L;
+            }
+            if (rm1 >= 0) {
+                float L = 0.f;
+                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 2u) % 3u][w];
+                P.loss[rm1] = L;
             }
         }
     }
@@ -439,8 +767,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
             mbar_init(&S.empty[s], NCW);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&S.xbar[b], (uint32_t)c);
-            mbar_init(&S.lbar[b], (uint32_t)c);
+            mbar_init(&S.xbar[b], 1u);      // the local expect_tx; the peers' data completes the bytes
+            mbar_init(&S.lbar[b], 1u);
         }
         S.abort = 0;
         S.issued = 0;
@@ -452,12 +780,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
 
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
-            producer<OP>(P, S, rank, cid, ncl);
+            producer<OP, RES>(P, S, rank, cid, ncl);
             drain(S);
         }
         __syncwarp();
     } else {
-        consumer<OP, RES>(P, S, rank, cid, ncl);
+        if (RES) consumer_self<OP>(P, S, rank, cid, ncl);
+        else consumer<OP, false>(P, S, rank, cid, ncl);
     }
     // no CTA may leave while a peer can still write into its shared memory
     if (c > 1) cluster_sync_all();
@@ -516,30 +845,42 @@ cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// Occupancy answers per (device, kernel, cluster size), queried once: the query costs
+// tens of microseconds, far more than a launch.
+std::atomic<int> g_max_clusters[kMaxDev][8][kMaxCluster + 1];
+
 int row_max_clusters(int op, bool resident, int c) {
     const void* fn = kernel_for(op, resident);
-    if (!fn || prepare(fn, slot_of(op, resident)) != cudaSuccess) return 0;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int slot = slot_of(op, resident);
+    if (!fn || c < 1 || c > kMaxCluster || prepare(fn, slot) != cudaSuccess) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const int cached = g_max_clusters[dev][slot][c].load(std::memory_order_acquire);
+    if (cached > 0) return cached;
+    int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (c <= 1) return sms;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(c * sms), 1, 1);
-    cfg.blockDim = dim3(NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(Smem);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)c;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
+    int n = sms;
+    if (c > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(c * sms), 1, 1);
+        cfg.blockDim = dim3(NTHREADS, 1, 1);
+        cfg.dynamicSmemBytes = sizeof(Smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        if (n <= 0) n = -1;         // remember "does not fit" too
     }
-    return n;
+    g_max_clusters[dev][slot][c].store(n, std::memory_order_release);
+    return n > 0 ? n : 0;
 }
 
 unsigned int rows_watchdog(bool clear) {

@@ -4,7 +4,8 @@
 // mbarriers with transaction counts, 1-D bulk copies global -> shared
 // (cp.async.bulk, the TMA engine's untiled form), cluster ranks and
 // distributed shared memory, named barriers with a popcount, and the
-// global nanosecond timer used to bound every wait.
+// bounded waits (a wait that has not completed after ~2 s is a bug: the kernel
+// records it and unwinds instead of hanging the GPU).
 #pragma once
 
 #include <cstdint>
@@ -13,9 +14,6 @@
 
 namespace vl {
 
-// A wait that has not completed after this long is a bug: the kernel records it
-// and unwinds instead of hanging the GPU.
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 
@@ -23,11 +21,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 // 2^x on the special-function unit (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
@@ -74,21 +67,28 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// SM cycles after which a wait gives up (about two seconds at the GB300's clocks).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
+
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false if the wait gave up: either another thread of the CTA raised
-// *abort, or this wait ran past kWaitTimeoutNs (then it raises *abort and sets
-// *flag).  Every wait in the library goes through here.
+// *abort, or this wait ran past kWaitTimeoutCycles (then it raises *abort and
+// sets *flag).  Every wait in the library goes through here.  The fast path is
+// one try_wait (which itself suspends the thread for a while); the clock and the
+// abort flag are only read after many failed polls.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, volatile int* abort,
                                             unsigned int* flag) {
     const uint32_t b = smem_u32(bar);
-    if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity)) return true;
-        if ((it & 15u) == 0u) {
+        if ((it & 255u) == 255u) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitTimeoutCycles) {
                 *abort = 1;
                 atomicOr(flag, 1u);
                 return false;
@@ -100,9 +100,9 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, vola
 // Same wait without the abort check, for draining copies already in flight.
 __device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity) {
     const uint32_t b = smem_u32(bar);
-    const unsigned long long t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) return false;
     }
     return true;
 }
@@ -156,6 +156,18 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(a) : "memory");
+}
+
+// Asynchronous store into a peer CTA's shared memory that completes `bytes` of the
+// transaction count of the peer's mbarrier when the data has landed (no fence).
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 :: "r"(addr), "f"(a), "f"(b), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 :: "r"(addr), "f"(a), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_remote_release(uint32_t bar_cluster_addr) {

@@ -30,13 +30,14 @@ struct RowParams {
 enum RowOp : int { kCeFused = 0, kCeFwd = 1, kCeBwd = 2, kKl = 3 };
 
 // Row-engine geometry limits (rows.cu).
-constexpr int kTileF = 2048;              // floats per pipeline tile (8 KB)
+constexpr int kConsumerWarps = 15;        // + one producer warp: 16 warps, up to 128 registers a thread
+constexpr int kTileF = 4 * 32 * kConsumerWarps;   // floats per pipeline tile: one float4 per consumer thread
 constexpr int kSlots = 24;                // tiles in the shared-memory ring
 constexpr int kMaxCluster = 8;
-constexpr long long kResidentMax = (long long)kSlots * kTileF;   // floats of one row part held on chip
 
-// Launch `op` over P; `resident` selects the mode that computes the row statistics
-// from the staged row (CE fused, self-contained KL).  Returns a CUDA error code.
+// Launch `op` over P; `resident` selects the self-contained mode that computes the
+// row statistics itself (CE fused, KL without given statistics).  Returns a CUDA
+// error code.
 cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters, cudaStream_t st);
 
 // Max active clusters of size c for the row kernel of `op` on the current device.

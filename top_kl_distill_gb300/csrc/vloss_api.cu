@@ -2,8 +2,9 @@
 // (acc_add, windowed mean).  Declarations and contracts: include/vloss.h.
 #include "vl_device.cuh"
 #include "vl_internal.h"
-#include "../../include/vloss.h"
+#include "vloss.h"
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -58,15 +59,23 @@ vl_status check_slice(int64_t col0, int64_t ncols, int64_t V, const char* fn) {
 }
 
 int num_sms() {
+    static std::atomic<int> cache[64];
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_acquire);
+        if (c > 0) return c;
+    }
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_release);
     return sms;
 }
 
-// Cluster size for a resident-mode launch: the smallest that fits a row part on
-// chip, raised while the estimated time (rows per cluster x part length, plus a
-// fixed per-row cost for the exchange) drops.  VLOSS_CLUSTER=c overrides it.
+// Grid of a launch.  Streaming modes: one CTA per SM (or per row when there are
+// fewer rows).  Self-contained mode: a row may be split over a cluster of c CTAs;
+// c is chosen from the estimated time, rows per cluster x (columns per CTA + a
+// fixed per-row cost of the cluster exchange), which favours c > 1 only when
+// rows are scarce.  VLOSS_CLUSTER=c overrides the choice.
 struct Grid {
     int csize;
     int nclusters;
@@ -78,25 +87,28 @@ Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
         long long g = rows < sms ? rows : sms;
         return Grid{1, (int)(g > 0 ? g : 1)};
     }
-    const long long body = ncols;   // upper bound of the aligned body
-    int cmin = (int)((body + kResidentMax - 1) / kResidentMax);
-    if (cmin < 1) cmin = 1;
-    if (cmin > kMaxCluster) return Grid{0, 0};
-    int forced = 0;
-    if (const char* e = std::getenv("VLOSS_CLUSTER")) forced = std::atoi(e);
-    if (forced >= cmin && forced <= kMaxCluster) {
+    // the KL loss of a row is reduced inside one CTA: no cluster split
+    if (op == kKl) {
+        long long g = rows < sms ? rows : sms;
+        return Grid{1, (int)(g > 0 ? g : 1)};
+    }
+    static const int forced = [] {
+        const char* e = std::getenv("VLOSS_CLUSTER");
+        return e ? std::atoi(e) : 0;
+    }();
+    if (forced >= 1 && forced <= kMaxCluster) {
         const int n = row_max_clusters(op, resident, forced);
         if (n > 0) return Grid{forced, (int)(rows < n ? rows : n)};
     }
+    const double exchange = 4.0 * kTileF;
     Grid best{0, 0};
     double best_cost = 0;
-    for (int c = cmin; c <= kMaxCluster; ++c) {
+    for (int c = 1; c <= kMaxCluster; ++c) {
         const int n = row_max_clusters(op, resident, c);
         if (n <= 0) continue;
         const long long ncl = rows < n ? rows : n;
         const long long waves = (rows + ncl - 1) / ncl;
-        const double part = (double)((ncols + c - 1) / c);
-        const double cost = (double)waves * (part + (c > 1 ? (double)kTileF : 0.0));
+        const double cost = (double)waves * ((double)((ncols + c - 1) / c) + (c > 1 ? exchange : 0.0));
         if (best.csize == 0 || cost < best_cost * 0.98) {
             best = Grid{c, (int)(ncl > 0 ? ncl : 1)};
             best_cost = cost;
@@ -181,9 +193,7 @@ RowParams base_params(float* logits, int64_t ld, int64_t ntok, int64_t V) {
 
 vl_status run_rows(int op, bool resident, RowParams& P, long long rows, const char* fn, cudaStream_t st) {
     const Grid g = choose_grid(op, resident, rows, P.ncols);
-    if (g.csize == 0)
-        return fail(VL_EUNSUPPORTED, "%s: a row of %lld columns does not fit %d CTAs of %lld floats", fn,
-                    (long long)P.ncols, kMaxCluster, (long long)kResidentMax);
+    if (g.csize == 0) return fail(VL_ELAUNCH, "%s: no launch configuration fits this device", fn);
     P.csize = g.csize;
     const cudaError_t e = launch_rows(op, resident, P, g.nclusters, st);
     if (e != cudaSuccess) return cuda_fail(e, fn);
@@ -274,30 +284,17 @@ vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const 
     if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
     const cudaStream_t st = as_stream(stream);
     if (ntok > 0) {
-        if (V > (long long)kMaxCluster * kResidentMax) {
-            // too long to stage on chip: statistics pass, then the in-place pass
-            if (stats == nullptr)
-                return fail(VL_EUNSUPPORTED, "%s: V > %lld needs the stats buffer", fn,
-                            (long long)kMaxCluster * kResidentMax);
-            if ((s = vl_ce_fwd(logits, ld, ntok, V, labels, loss_start, loss_end, loss, lse, stats, nullptr, err,
-                               stream)))
-                return s;
-            if ((s = vl_ce_bwd_inplace(logits, ld, ntok, V, 0, V, labels, nullptr, stats, loss_start, loss_end,
-                                       scale, nullptr, nullptr, stream)))
-                return s;
-        } else {
-            RowParams P = base_params(logits, ld, ntok, V);
-            P.labels = labels;
-            P.ls = loss_start;
-            P.le = loss_end;
-            P.cg = scale;
-            P.ce_coef = scale;
-            P.loss = loss;
-            P.lse_out = lse;
-            P.stats_out = stats;
-            P.err = err;
-            if ((s = run_rows(kCeFused, true, P, ntok, fn, st))) return s;
-        }
+        RowParams P = base_params(logits, ld, ntok, V);
+        P.labels = labels;
+        P.ls = loss_start;
+        P.le = loss_end;
+        P.cg = scale;
+        P.ce_coef = scale;
+        P.loss = loss;
+        P.lse_out = lse;
+        P.stats_out = stats;
+        P.err = err;
+        if ((s = run_rows(kCeFused, true, P, ntok, fn, st))) return s;
     }
     if (mean) {
         const cudaError_t e = launch_mean(loss, loss_start, loss_end, mean, st);
@@ -340,9 +337,6 @@ vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
     P.stats_in = stats_in;
     P.loss = loss;
     P.err = err;
-    if (self && V > (long long)kMaxCluster * kResidentMax)
-        return fail(VL_EUNSUPPORTED, "%s: V > %lld: compute stats with vl_ce_fwd and pass stats_in", fn,
-                    (long long)kMaxCluster * kResidentMax);
     const long long rows = loss_end - loss_start;
     return run_rows(kKl, self, P, rows > 0 ? rows : 1, fn, as_stream(stream));
 }

@@ -166,14 +166,11 @@ def logits(w: Workload, r0: int = 0, r1: int | None = None, out: np.ndarray | No
         def blk(b, n):
             g = _gen(w.seed, _T_LOGITS, b)
             gp = _gen(w.seed, _T_PERM, b)
-            x = g.standard_normal((n, V), dtype=np.float32).astype(np.float64)
-            x *= ex["sigma"]
-            for i in range(n):
-                x[i] += ex["jitter"] * gp.permutation(V)
-            x = x.astype(np.float32)
-            for i in range(n):
-                make_distinct(x[i])
-            return x
+            x = g.standard_normal((n, V), dtype=np.float32)
+            x *= np.float32(ex["sigma"])
+            perm = gp.permuted(np.broadcast_to(np.arange(V, dtype=np.int32), (n, V)), axis=1)
+            x += perm.astype(np.float32) * np.float32(ex["jitter"])
+            return make_distinct_rows(x)
     elif "t_dof" in ex:
         def blk(b, n):
             g = _gen(w.seed, _T_LOGITS, b)
@@ -190,21 +187,27 @@ def logits(w: Workload, r0: int = 0, r1: int | None = None, out: np.ndarray | No
     return _fill_rows(out, r0, r1, w.ntok, blk, threads)
 
 
-def make_distinct(row: np.ndarray) -> np.ndarray:
-    """Nudge equal fp32 values of ``row`` upward (nextafter) until all differ.
+def make_distinct_rows(x: np.ndarray) -> np.ndarray:
+    """Nudge equal fp32 values within each row of ``x`` upward (nextafter) until all differ.
 
-    In place.  The value that keeps its place is the one at the lowest column;
+    In place.  Among equal values the one at the lowest column keeps its value;
     each later duplicate moves up by one ulp and the check repeats.
     """
-    assert row.dtype == np.float32
+    assert x.dtype == np.float32 and x.ndim == 2
     while True:
-        order = np.argsort(row, kind="stable")
-        srt = row[order]
-        dup = np.nonzero(srt[1:] == srt[:-1])[0] + 1
-        if dup.size == 0:
-            return row
-        idx = order[dup]
-        row[idx] = np.nextafter(row[idx], np.float32(np.inf))
+        order = np.argsort(x, axis=1, kind="stable")
+        srt = np.take_along_axis(x, order, axis=1)
+        r, c = np.nonzero(srt[:, 1:] == srt[:, :-1])
+        if r.size == 0:
+            return x
+        cols = order[r, c + 1]
+        x[r, cols] = np.nextafter(x[r, cols], np.float32(np.inf))
+
+
+def make_distinct(row: np.ndarray) -> np.ndarray:
+    """make_distinct_rows for one row."""
+    make_distinct_rows(row.reshape(1, -1))
+    return row
 
 
 # ---------------------------------------------------------------- teacher
