@@ -11,7 +11,7 @@
 //   * warp 0 (one lane) is the producer: it streams each CTA's body through a
 //     ring of kSlots tiles of kTileF floats with 1-D bulk copies (TMA) signalled
 //     on per-slot mbarriers; warps 1..15 are consumers.  A consumer thread owns
-//     float4 number `ct` of every tile.
+//     float4s ct, ct + NCT, ... (kVec of them) of every tile.
 //
 // Modes
 //   self-contained (CE fused, KL without given statistics): the producer streams
@@ -53,7 +53,7 @@ constexpr int BMPW = 1024;              // words of the self-contained support b
 constexpr int KSELF = 1024;             // teacher support per row, self-contained mode
 constexpr uint32_t kBarConsumers = 1;   // named barrier id used by consumers only
 
-static_assert(kTileF / 4 == NCT, "one float4 of each tile per consumer thread");
+static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
 static_assert(KMAX >= 1024, "the C ABI promises k <= 1024");
 
 __device__ unsigned int g_watchdog;
@@ -317,7 +317,11 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
                 wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
                 const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
-                if (ct < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][ct * 4]));
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    const int j = u * NCT + ct;
+                    if (j < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][j * 4]));
+                }
                 if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
                 if (ct == LT) gather(lab, t, S.ring[slot]);
                 __syncwarp();
@@ -368,11 +372,15 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
                 wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
                 const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
-                if (ct < n4) {
-                    const float4 x = ld_shared_v4(&S.ring[slot][ct * 4]);
-                    const float4 o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
-                                                 c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
-                    st_global_v4(rowp + pt.b0 + t * kTileF + 4 * ct, o);
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    const int j = u * NCT + ct;
+                    if (j < n4) {
+                        const float4 x = ld_shared_v4(&S.ring[slot][j * 4]);
+                        const float4 o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
+                                                     c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
+                        st_global_v4(rowp + pt.b0 + t * kTileF + 4 * j, o);
+                    }
                 }
                 if (!RES) {
                     if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
@@ -503,54 +511,58 @@ __device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pendi
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
         const int n4 = min(kTileF, w.pt.bn - t * kTileF) >> 2;
-        const int c0 = w.pt.b0 + t * kTileF + 4 * ct;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), o = x;
-        uint32_t hit = 0u;
-        if (ct < n4) {
-            x = ld_shared_v4(&S.ring[slot][ct * 4]);
-            o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS), c1 * soft(x.z, w.m, w.lnS),
-                            c1 * soft(x.w, w.m, w.lnS));
-            if (w.inwin) {
-                const unsigned d = (unsigned)(w.jl - c0);
-                if (d < 4u) {
-                    const float xs = d == 0 ? x.x : d == 1 ? x.y : d == 2 ? x.z : x.w;
-                    sub_at(o, d, P.ce_coef);
-                    if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int j = u * NCT + ct;
+            const int c0 = w.pt.b0 + t * kTileF + 4 * j;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f), o = x;
+            uint32_t hit = 0u;
+            if (j < n4) {
+                x = ld_shared_v4(&S.ring[slot][j * 4]);
+                o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS), c1 * soft(x.z, w.m, w.lnS),
+                                c1 * soft(x.w, w.m, w.lnS));
+                if (w.inwin) {
+                    const unsigned d = (unsigned)(w.jl - c0);
+                    if (d < 4u) {
+                        const float xs = d == 0 ? x.x : d == 1 ? x.y : d == 2 ? x.z : x.w;
+                        sub_at(o, d, P.ce_coef);
+                        if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
+                    }
+                }
+                if (kKL && w.inwin) {
+                    const uint32_t bi = (uint32_t)(t * NCT * kVec + j) >> gs;   // float4 index in the body
+                    hit = (S.bmp[w.b3][bi >> 5] >> (bi & 31u)) & 1u;
                 }
             }
             if (kKL && w.inwin) {
-                const uint32_t bi = (uint32_t)(t * NCT + ct) >> gs;
-                hit = (S.bmp[w.b3][bi >> 5] >> (bi & 31u)) & 1u;
-            }
-        }
-        if (kKL && w.inwin) {
-            // a flagged float4 holds a support id: the whole warp walks the support list
-            uint32_t hits = __ballot_sync(0xffffffffu, hit != 0u);
-            while (hits) {
-                const int src = __ffs(hits) - 1;
-                hits &= hits - 1u;
-                const int cs = __shfl_sync(0xffffffffu, c0, src);
-                const float x0 = __shfl_sync(0xffffffffu, x.x, src), x1 = __shfl_sync(0xffffffffu, x.y, src);
-                const float x2 = __shfl_sync(0xffffffffu, x.z, src), x3 = __shfl_sync(0xffffffffu, x.w, src);
-                float4 corr = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j0 = 0; j0 < P.k; j0 += 32) {
-                    const int j = j0 + lane;
-                    const unsigned de = j < P.k ? (unsigned)(S.ecol[w.b3][j] - cs) : 4u;
-                    if (de < 4u) {
-                        const float p = S.ep[w.b3][j];
-                        const float xs = de == 0 ? x0 : de == 1 ? x1 : de == 2 ? x2 : x3;
-                        sub_at(corr, de, -P.coef * p);
-                        if (p > 0.f) lacc += p * (logf(p) - ((xs - w.m) - w.lnS));
+                // a flagged float4 holds a support id: the whole warp walks the support list
+                uint32_t hits = __ballot_sync(0xffffffffu, hit != 0u);
+                while (hits) {
+                    const int src = __ffs(hits) - 1;
+                    hits &= hits - 1u;
+                    const int cs = __shfl_sync(0xffffffffu, c0, src);
+                    const float x0 = __shfl_sync(0xffffffffu, x.x, src), x1 = __shfl_sync(0xffffffffu, x.y, src);
+                    const float x2 = __shfl_sync(0xffffffffu, x.z, src), x3 = __shfl_sync(0xffffffffu, x.w, src);
+                    float4 corr = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int j0 = 0; j0 < P.k; j0 += 32) {
+                        const int e = j0 + lane;
+                        const unsigned de = e < P.k ? (unsigned)(S.ecol[w.b3][e] - cs) : 4u;
+                        if (de < 4u) {
+                            const float p = S.ep[w.b3][e];
+                            const float xs = de == 0 ? x0 : de == 1 ? x1 : de == 2 ? x2 : x3;
+                            sub_at(corr, de, -P.coef * p);
+                            if (p > 0.f) lacc += p * (logf(p) - ((xs - w.m) - w.lnS));
+                        }
                     }
+                    corr.x = warp_sum(corr.x);
+                    corr.y = warp_sum(corr.y);
+                    corr.z = warp_sum(corr.z);
+                    corr.w = warp_sum(corr.w);
+                    if (lane == src) { o.x -= corr.x; o.y -= corr.y; o.z -= corr.z; o.w -= corr.w; }
                 }
-                corr.x = warp_sum(corr.x);
-                corr.y = warp_sum(corr.y);
-                corr.z = warp_sum(corr.z);
-                corr.w = warp_sum(corr.w);
-                if (lane == src) { o.x -= corr.x; o.y -= corr.y; o.z -= corr.z; o.w -= corr.w; }
             }
+            if (j < n4) st_global_v4(w.rowp + c0, o);
         }
-        if (ct < n4) st_global_v4(w.rowp + c0, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
     }
@@ -661,7 +673,11 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
             wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
             const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
-            if (ct < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][ct * 4]));
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int j = u * NCT + ct;
+                if (j < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][j * 4]));
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
         }

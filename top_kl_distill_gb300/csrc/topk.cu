@@ -7,17 +7,16 @@
 // share a residue class and breaks ties arbitrarily.  This kernel is exact, with
 // ties going to the lower column:
 //
-//   * one persistent CTA per SM streams its rows through a ring of 8 KB tiles
+//   * one persistent CTA per SM streams its rows through a ring of 15 KB tiles
 //     (1-D bulk copies, producer warp + 15 consumer warps, as the row engine);
 //   * each consumer warp owns a region of the shared candidate buffer.  A value
-//     enters its warp's region when it is above the running threshold T (the
-//     k-th best value kept so far).  Columns arrive in increasing order, so a
-//     value equal to T always loses to the candidate already held and "x > T"
-//     is the exact admission test;
+//     enters its warp's region when it is at or above the running threshold T
+//     (the k-th best value kept so far); ties with T are decided by the
+//     composite order (value desc, id asc) at the next selection;
 //   * when a region could overflow, an exact radix select over order-preserving
 //     32-bit keys (-0.0 folded into +0.0; 8-bit digits over the key range
 //     present, warp-private histograms; then over the ids of tied keys) keeps the
-//     best k and raises T;
+//     best k, spreads them evenly over the regions and raises T;
 //   * at the end of the row the k survivors are ordered by (value desc, id asc)
 //     and written with their probabilities.
 #include "vl_device.cuh"
@@ -31,7 +30,7 @@ namespace {
 constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
-constexpr int kSlotsT = 14;          // ring tiles
+constexpr int kSlotsT = 7;           // ring tiles (105 KB)
 constexpr int RW = 512;              // candidate entries per consumer warp
 constexpr int CB = RW * NCW;         // candidate buffer entries
 constexpr int NPER = RW / 32;        // candidates per lane while compacting
@@ -41,8 +40,8 @@ constexpr int NBIN = 1 << DB;
 constexpr int PER_TILE = kTileF / NCW;   // most candidates a warp can add per tile
 constexpr uint32_t kBar = 1;
 
-static_assert(kTileF / 4 == NCT, "one float4 of each tile per consumer thread");
-static_assert(((KMAXT + NCW - 1) / NCW) + 6 + 2 * PER_TILE <= RW, "survivors plus two tiles fit a region");
+static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
+static_assert(((KMAXT + NCW - 1) / NCW) + 6 + PER_TILE <= RW, "survivors plus one tile fit a region");
 
 __device__ unsigned int g_watchdog;
 
@@ -323,23 +322,31 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlotsT;
             wait_parity<false>(&S.full[slot], (gt / kSlotsT) & 1u, &S.abort, &g_watchdog);
             const int n4 = min(kTileF, bt - t * kTileF) >> 2;
-            const bool active = ct < n4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (active) v = ld_shared_v4(&S.ring[slot][ct * 4]);
+            float4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int j = u * NCT + ct;
+                v[u] = j < n4 ? ld_shared_v4(&S.ring[slot][j * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
-            // most float4s hold nothing above the threshold: one vote per warp
-            const bool any = active && (!armed || fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) > T);
-            if (__any_sync(0xffffffffu, any)) {
-                const uint32_t c0 = (uint32_t)(h + t * kTileF + 4 * ct);
-                wappend(S, cw, cnt, any && (!armed || v.x > T), v.x, c0);
-                wappend(S, cw, cnt, any && (!armed || v.y > T), v.y, c0 + 1);
-                wappend(S, cw, cnt, any && (!armed || v.z > T), v.z, c0 + 2);
-                wappend(S, cw, cnt, any && (!armed || v.w > T), v.w, c0 + 3);
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int j = u * NCT + ct;
+                const bool active = j < n4;
+                // most float4s hold nothing at or above the threshold: one vote per warp
+                const bool any = active && (!armed || fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T);
+                if (__any_sync(0xffffffffu, any)) {
+                    const uint32_t c0 = (uint32_t)(h + t * kTileF + 4 * j);
+                    wappend(S, cw, cnt, any && (!armed || v[u].x >= T), v[u].x, c0);
+                    wappend(S, cw, cnt, any && (!armed || v[u].y >= T), v[u].y, c0 + 1);
+                    wappend(S, cw, cnt, any && (!armed || v[u].z >= T), v[u].z, c0 + 2);
+                    wappend(S, cw, cnt, any && (!armed || v[u].w >= T), v[u].w, c0 + 3);
+                }
             }
-            // every other tile: compact when some region could overflow within two tiles
-            if ((t & 1) == 1 && t + 1 < nt) {
-                const uint32_t full = named_sync_popc(kBar, NCT, lane == 0 && cnt + 2 * PER_TILE > (uint32_t)RW);
+            // compact when some region could overflow on the next tile
+            if (t + 1 < nt) {
+                const uint32_t full = named_sync_popc(kBar, NCT, lane == 0 && cnt + PER_TILE > (uint32_t)RW);
                 if (full) {
                     if (lane == 0) S.wcnt[cw] = cnt;
                     named_sync(kBar, NCT);
@@ -375,16 +382,27 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         // ---- order the k survivors by (value desc, id asc)
         const uint32_t K = (uint32_t)k;
         if (K <= (uint32_t)NCT) {
+            // rank of each survivor among all k by the composite key, built once
+            unsigned long long* ck = reinterpret_cast<unsigned long long*>(S.cval);
+            const bool mine = (uint32_t)ct < K;
             float mv = 0.f;
             uint32_t mi = 0;
             unsigned long long mc = 0;
-            const bool mine = (uint32_t)ct < K;
-            if (mine) { mv = S.okey[ct]; mi = S.oid[ct]; mc = comp(mv, mi); }
-            uint32_t pos = 0;
-            if (mine)
-                for (uint32_t j = 0; j < K; ++j) pos += comp(S.okey[j], S.oid[j]) > mc ? 1u : 0u;
+            if (mine) { mv = S.okey[ct]; mi = S.oid[ct]; mc = comp(mv, mi); ck[ct] = mc; }
             named_sync(kBar, NCT);
-            if (mine) { S.okey[pos] = mv; S.oid[pos] = mi; }
+            if (mine) {
+                uint32_t p0 = 0, p1 = 0, p2 = 0, p3 = 0, j = 0;
+                for (; j + 4 <= K; j += 4) {
+                    p0 += ck[j] > mc;
+                    p1 += ck[j + 1] > mc;
+                    p2 += ck[j + 2] > mc;
+                    p3 += ck[j + 3] > mc;
+                }
+                for (; j < K; ++j) p0 += ck[j] > mc;
+                const uint32_t pos = (p0 + p1) + (p2 + p3);
+                S.okey[pos] = mv;      // every thread read its own entry before the barrier
+                S.oid[pos] = mi;
+            }
             named_sync(kBar, NCT);
         } else {
             uint32_t Kp = 1;
