@@ -25,9 +25,12 @@
 //   streaming (CE backward, KL with given statistics): pass B only.
 //   reduce    (CE forward): pass A only.
 //
-// Sparse columns (the label, the teacher's top-k ids) are fixed up after the bulk
-// store of the row and a barrier: their values are gathered from the staged tiles
-// as they pass, their gradient is rewritten, and their loss terms are reduced.
+// Sparse columns (the label, the teacher's top-k ids).  Streaming mode gathers their
+// logits from the staged tiles as they pass and rewrites their gradient after the
+// bulk store of the row and a barrier.  Self-contained mode folds the label into
+// pass B, gathers the support logits from global memory before pass A (the row is
+// not written until after it) for the KL loss, and adds -coef * p_q at the support
+// columns with reduction adds after a barrier that follows the row's pass B.
 //
 // Sources: aprender-train wgpu_cross_entropy.rs (module doc, forward_async,
 // backward: loss = lse - s[label], gradient scale * (softmax - onehot), loss
@@ -49,8 +52,11 @@ constexpr int NTHREADS = NCT + 32;      // + the producer warp
 constexpr int EPT = 3;                  // teacher support entries per consumer thread
 constexpr int KMAX = EPT * NCT;         // teacher support per row
 constexpr int LT = NCT - 1;             // the consumer thread that handles the label
-constexpr int BMPW = 1024;              // words of the self-contained support bitmap
 constexpr int KSELF = 1024;             // teacher support per row, self-contained mode
+// A row's support is written before its pass A and scattered two rows later, after
+// the barrier that follows its pass B; four buffers keep the writer of row i + 2
+// behind the barrier of row i + 1, which every scatter of row i - 2 precedes.
+constexpr uint32_t kSupBufs = 4;
 constexpr uint32_t kBarConsumers = 1;   // named barrier id used by consumers only
 
 static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
@@ -74,11 +80,10 @@ struct alignas(128) Smem {
             float kp[2][KMAX];               // probability per entry
             float ks[2][KMAX];               // the logit at that column, gathered as its tile passes
         };
-        struct {                        // self-contained mode: three rows in flight
-            uint32_t bmp[3][BMPW];           // one bit per float4 group that holds a support id
-            int ecol[3][KSELF];              // support column (slice-relative; -1 elsewhere)
-            float ep[3][KSELF];
-            float wl3[3][NCW];               // KL loss per warp, reduced one row later
+        struct {                        // self-contained mode: support of the last kSupBufs rows
+            int ecol[kSupBufs][KSELF];       // support column (slice-relative; -1 elsewhere)
+            float ep[kSupBufs][KSELF];
+            float wl2[2][NCW];               // KL loss per warp, summed one row later
         };
     };
     int abort;
@@ -485,8 +490,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
 
 // ---------------------------------------------------------------- self-contained consumer
 
-// Pass B of a row whose statistics are known: the gradient tile by tile, the label
-// and the teacher support corrected inline, the KL loss terms accumulated.
+// A row whose pass A is done and whose pass B is still to come.
 struct Pending {
     long long r;
     float* rowp;
@@ -495,18 +499,17 @@ struct Pending {
     bool inwin, bad;
     int jl;          // slice-relative label column, -1 when none or outside this CTA's columns
     float m, lnS;
-    uint32_t b3;     // buffer of its support, bitmap and KL loss
     bool has_ht;
     int jht;
     float ht;
 };
 
+// Pass B of a row whose statistics are known: the gradient tile by tile with the
+// label's one-hot folded in.  The teacher support is left to scatter_support.
 template <int OP>
-__device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
-                                        int rank, int gs) {
-    constexpr bool kKL = OP == kKl;
+__device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
+                                       int rank) {
     const float c1 = w.inwin ? P.cg : 0.f;
-    float lacc = 0.f;
     for (int t = 0; t < w.nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
@@ -514,13 +517,11 @@ __device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pendi
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int j = u * NCT + ct;
-            const int c0 = w.pt.b0 + t * kTileF + 4 * j;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f), o = x;
-            uint32_t hit = 0u;
             if (j < n4) {
-                x = ld_shared_v4(&S.ring[slot][j * 4]);
-                o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS), c1 * soft(x.z, w.m, w.lnS),
-                                c1 * soft(x.w, w.m, w.lnS));
+                const int c0 = w.pt.b0 + t * kTileF + 4 * j;
+                const float4 x = ld_shared_v4(&S.ring[slot][j * 4]);
+                float4 o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS),
+                                       c1 * soft(x.z, w.m, w.lnS), c1 * soft(x.w, w.m, w.lnS));
                 if (w.inwin) {
                     const unsigned d = (unsigned)(w.jl - c0);
                     if (d < 4u) {
@@ -529,39 +530,8 @@ __device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pendi
                         if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
                     }
                 }
-                if (kKL && w.inwin) {
-                    const uint32_t bi = (uint32_t)(t * NCT * kVec + j) >> gs;   // float4 index in the body
-                    hit = (S.bmp[w.b3][bi >> 5] >> (bi & 31u)) & 1u;
-                }
+                st_global_v4(w.rowp + c0, o);
             }
-            if (kKL && w.inwin) {
-                // a flagged float4 holds a support id: the whole warp walks the support list
-                uint32_t hits = __ballot_sync(0xffffffffu, hit != 0u);
-                while (hits) {
-                    const int src = __ffs(hits) - 1;
-                    hits &= hits - 1u;
-                    const int cs = __shfl_sync(0xffffffffu, c0, src);
-                    const float x0 = __shfl_sync(0xffffffffu, x.x, src), x1 = __shfl_sync(0xffffffffu, x.y, src);
-                    const float x2 = __shfl_sync(0xffffffffu, x.z, src), x3 = __shfl_sync(0xffffffffu, x.w, src);
-                    float4 corr = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int j0 = 0; j0 < P.k; j0 += 32) {
-                        const int e = j0 + lane;
-                        const unsigned de = e < P.k ? (unsigned)(S.ecol[w.b3][e] - cs) : 4u;
-                        if (de < 4u) {
-                            const float p = S.ep[w.b3][e];
-                            const float xs = de == 0 ? x0 : de == 1 ? x1 : de == 2 ? x2 : x3;
-                            sub_at(corr, de, -P.coef * p);
-                            if (p > 0.f) lacc += p * (logf(p) - ((xs - w.m) - w.lnS));
-                        }
-                    }
-                    corr.x = warp_sum(corr.x);
-                    corr.y = warp_sum(corr.y);
-                    corr.z = warp_sum(corr.z);
-                    corr.w = warp_sum(corr.w);
-                    if (lane == src) { o.x -= corr.x; o.y -= corr.y; o.z -= corr.z; o.w -= corr.w; }
-                }
-            }
-            if (j < n4) st_global_v4(w.rowp + c0, o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -569,18 +539,9 @@ __device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pendi
     g += (uint32_t)w.nt;
     if (w.has_ht) {
         float o = c1 * soft(w.ht, w.m, w.lnS);
-        if (w.inwin) {
-            if (w.jht == w.jl) {
-                o -= P.ce_coef;
-                if (OP == kCeFused) P.loss[w.r] = (w.m - w.ht) + w.lnS;
-            }
-            if (kKL)
-                for (int e = 0; e < P.k; ++e)
-                    if (S.ecol[w.b3][e] == w.jht) {
-                        const float p = S.ep[w.b3][e];
-                        o -= P.coef * p;
-                        if (p > 0.f) lacc += p * (logf(p) - ((w.ht - w.m) - w.lnS));
-                    }
+        if (w.inwin && w.jht == w.jl) {
+            o -= P.ce_coef;
+            if (OP == kCeFused) P.loss[w.r] = (w.m - w.ht) + w.lnS;
         }
         w.rowp[w.jht] = o;
     }
@@ -588,7 +549,17 @@ __device__ __forceinline__ float pass_b(const RowParams& P, Smem& S, const Pendi
         if (!w.inwin) P.loss[w.r] = 0.f;
         else if (w.bad) P.loss[w.r] = __int_as_float(0x7fc00000);
     }
-    return lacc;
+}
+
+// -coef * p_q added at every support column of loaded row r (buffer sb).  Reduction
+// adds, so repeated ids sum.  Runs after a barrier that follows the row's pass B:
+// the barrier orders every thread's gradient store before these adds.
+__device__ __forceinline__ void scatter_support(const RowParams& P, const Smem& S, long long r, uint32_t sb, int ct) {
+    float* rowp = P.x + r * P.ld + P.col0;
+    for (int q = ct; q < P.k; q += NCT) {
+        const int col = S.ecol[sb][q];
+        if (col >= 0) atomicAdd(rowp + col, -P.coef * S.ep[sb][q]);
+    }
 }
 
 template <int OP>
@@ -599,12 +570,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const int c = P.csize;
     const int ncols = (int)P.ncols;
     const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
-    // bitmap granularity: 2^gs float4 per bit, so that any row part fits BMPW words
-    int gs = 0;
-    while ((((ncols + 3) >> 2) >> gs) > BMPW * 32) ++gs;
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
-    long long rm1 = -1, rm2 = -1;      // rows of the last two passes B, for the deferred KL loss
-    if (kKL) for (int i = ct; i < BMPW; i += NCT) S.bmp[0][i] = 0u;
+    long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (loss, support scatter owed)
     uint32_t nlab = 0, nid = 0;
     float np = 0.f;
     auto prefetch = [&](long long rr) {
@@ -628,14 +595,13 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             if (ct == 0 && rank == 0) P.loss[r] = 0.f;
             continue;
         }
-        const uint32_t b3 = li % 3u;
+        const uint32_t sb = li % kSupBufs;
         Pending cur;
         cur.r = r;
         cur.rowp = rowp;
         cur.pt = pt;
         cur.nt = (pt.bn + kTileF - 1) / kTileF;
         cur.inwin = inwin;
-        cur.b3 = b3;
         cur.jl = -1;
         cur.bad = false;
         if (has_label) {
@@ -646,20 +612,37 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             }
         }
         if (cur.bad && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
-        if (kKL && inwin) {
+        // teacher support entries q = ct + i * NCT: column and probability to shared
+        // memory for the scatter, the logit gathered now -- nothing of the row is
+        // written before the barrier that ends its pass A -- for the loss
+        int scol[EPT];
+        float sp[EPT], sx[EPT];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            scol[i] = -1;
+            sp[i] = 0.f;
+            sx[i] = 0.f;
+        }
+        if (kKL) {
+#pragma unroll
             for (int i = 0; i < EPT; ++i) {
                 const int q = ct + i * NCT;
-                if (q >= P.k) break;
-                const uint32_t id = i == 0 ? id0 : P.tid[r * P.k + q];
-                int col = -1;
-                if ((long long)id >= P.V) {
-                    if (rank == 0 && P.err) atomicAdd(P.err, 1);
-                } else {
-                    const long long j = (long long)id - P.col0;
-                    if (j >= pt.lo && j < pt.hi) col = (int)j;
+                if (q < P.k) {
+                    const uint32_t id = i == 0 ? id0 : P.tid[r * P.k + q];
+                    const float p = i == 0 ? p0 : P.tp[r * P.k + q];
+                    int col = -1;
+                    if ((long long)id >= P.V) {
+                        if (rank == 0 && P.err) atomicAdd(P.err, 1);
+                    } else {
+                        const long long j = (long long)id - P.col0;
+                        if (j >= pt.lo && j < pt.hi) col = (int)j;
+                    }
+                    S.ecol[sb][q] = col;
+                    S.ep[sb][q] = p;
+                    scol[i] = col;
+                    sp[i] = p;
+                    if (col >= 0) sx[i] = rowp[col];
                 }
-                S.ecol[b3][q] = col;
-                S.ep[b3][q] = i == 0 ? p0 : P.tp[r * P.k + q];
             }
         }
         cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
@@ -706,65 +689,40 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             if (P.lse_out) P.lse_out[r] = cur.m + cur.lnS;
             if (P.stats_out) { P.stats_out[2 * r] = cur.m; P.stats_out[2 * r + 1] = cur.lnS; }
         }
-        // ---- after this row's barrier: every pass B up to two rows back is done
         if (kKL) {
-            const uint32_t nb = (li + 1u) % 3u;
-            for (int i = ct; i < BMPW; i += NCT) S.bmp[nb][i] = 0u;
-            if (inwin) {
-                for (int i = 0; i < EPT; ++i) {
-                    const int q = ct + i * NCT;
-                    if (q >= P.k) break;
-                    const int col = S.ecol[b3][q];
-                    if (col >= pt.b0 && col < pt.b0 + pt.bn) {
-                        const uint32_t bi = (uint32_t)((col - pt.b0) >> 2) >> gs;
-                        atomicOr(&S.bmp[b3][bi >> 5], 1u << (bi & 31u));
-                    }
-                }
-            }
-            if (ct == 0 && rm1 >= 0) {           // pass B of loaded row li - 2 is done
+            // this row's loss terms from the gathered logits
+            float lacc = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPT; ++i)
+                if (scol[i] >= 0 && sp[i] > 0.f) lacc += sp[i] * (logf(sp[i]) - ((sx[i] - cur.m) - cur.lnS));
+            lacc = warp_sum(lacc);
+            if (lane == 0) S.wl2[li & 1u][cw] = lacc;
+            // past this row's barrier: the previous row's loss terms are all in, and
+            // pass B of the row two back is done
+            if (ct == 0 && rk1 >= 0) {
                 float L = 0.f;
-                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 1u) % 3u][w];
-                P.loss[rm1] = L;
+                for (int w = 0; w < NCW; ++w) L += S.wl2[(li + 1u) & 1u][w];
+                P.loss[rk1] = L;
             }
+            if (rk2 >= 0) scatter_support(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
         }
         // ---- pass B of the previous row
-        if (pend.r >= 0) {
-            float lacc = pass_b<OP>(P, S, pend, g, ct, lane, rank, gs);
-            if (kKL) {
-                lacc = warp_sum(lacc);
-                if (lane == 0) S.wl3[pend.b3][cw] = lacc;
-            }
-            rm2 = rm1;
-            rm1 = pend.r;
-        }
+        if (pend.r >= 0) pass_b<OP>(P, S, pend, g, ct, lane, rank);
         pend = cur;
+        rk2 = rk1;
+        rk1 = r;
         ++li;
     }
-    if (pend.r >= 0) {
-        named_sync(kBarConsumers, NCT);          // the last row's bitmap is set
-        float lacc = pass_b<OP>(P, S, pend, g, ct, lane, rank, gs);
-        if (kKL) {
-            lacc = warp_sum(lacc);
-            if (lane == 0) S.wl3[pend.b3][cw] = lacc;
-        }
-        rm2 = rm1;
-        rm1 = pend.r;
-    }
-    if (kKL) {
+    if (pend.r >= 0) pass_b<OP>(P, S, pend, g, ct, lane, rank);
+    if (kKL && li > 0) {
         named_sync(kBarConsumers, NCT);
         if (ct == 0) {
-            // rows li-2 and li-1 (in loaded order) still owe their loss
-            if (rm2 >= 0) {
-                float L = 0.f;
-                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 1u) % 3u][w];
-                P.loss[rm2] = L;
-            }
-            if (rm1 >= 0) {
-                float L = 0.f;
-                for (int w = 0; w < NCW; ++w) L += S.wl3[(li + 2u) % 3u][w];
-                P.loss[rm1] = L;
-            }
+            float L = 0.f;
+            for (int w = 0; w < NCW; ++w) L += S.wl2[(li - 1u) & 1u][w];
+            P.loss[rk1] = L;
         }
+        if (rk2 >= 0) scatter_support(P, S, rk2, (li - 2u) % kSupBufs, ct);
+        scatter_support(P, S, rk1, (li - 1u) % kSupBufs, ct);
     }
 }
 
