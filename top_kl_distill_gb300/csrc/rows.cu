@@ -142,6 +142,27 @@ __device__ __forceinline__ void sub_at(float4& o, unsigned d, float a) {
     else o.w -= a;
 }
 
+// (max, sum) update with kVec float4s (absent values are -inf): one max update,
+// independent exponentials summed as a tree.
+__device__ __forceinline__ void ms_addv(MaxSum& a, const float4 (&v)[kVec]) {
+    float mx = fmaxf(fmaxf(v[0].x, v[0].y), fmaxf(v[0].z, v[0].w));
+#pragma unroll
+    for (int u = 1; u < kVec; ++u) mx = fmaxf(mx, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+    if (mx > a.m) {
+        a.s *= ex2((a.m - mx) * kLog2e);
+        a.m = mx;
+    }
+    float e[kVec];
+#pragma unroll
+    for (int u = 0; u < kVec; ++u)
+        e[u] = (ex2((v[u].x - a.m) * kLog2e) + ex2((v[u].y - a.m) * kLog2e)) +
+               (ex2((v[u].z - a.m) * kLog2e) + ex2((v[u].w - a.m) * kLog2e));
+    float t = e[0];
+#pragma unroll
+    for (int u = 1; u < kVec; ++u) t += e[u];
+    a.s += t;
+}
+
 __device__ __forceinline__ float max4(const float4& v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
 
 // ---------------------------------------------------------------- producer
@@ -373,6 +394,10 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
         // ---- pass B: each tile turned into gradient as it lands (zeros outside the window)
         {
             const float c1 = inwin ? cg : 0.f;
+            // c1 * exp(d - lnS) = 2^(d * log2e - K), K = lnS * log2e - log2(c1), for c1 >= 0
+            const bool fold = c1 >= 0.f;
+            const float K = fold ? lnS * kLog2e - log2f(c1) : 0.f;
+            const uint64_t pol = l2_evict_first();
             for (int t = 0; t < nt; ++t) {
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
                 wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
@@ -382,9 +407,15 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                     const int j = u * NCT + ct;
                     if (j < n4) {
                         const float4 x = ld_shared_v4(&S.ring[slot][j * 4]);
-                        const float4 o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
-                                                     c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
-                        st_global_v4(rowp + pt.b0 + t * kTileF + 4 * j, o);
+                        float4 o;
+                        if (fold) {
+                            o = make_float4(ex2(fmaf(x.x - m, kLog2e, -K)), ex2(fmaf(x.y - m, kLog2e, -K)),
+                                            ex2(fmaf(x.z - m, kLog2e, -K)), ex2(fmaf(x.w - m, kLog2e, -K)));
+                        } else {
+                            o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
+                                            c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
+                        }
+                        st_global_v4_hint(rowp + pt.b0 + t * kTileF + 4 * j, o, pol);
                     }
                 }
                 if (!RES) {
@@ -510,18 +541,38 @@ template <int OP>
 __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
                                        int rank) {
     const float c1 = w.inwin ? P.cg : 0.f;
+    // c1 * exp(d - lnS) = 2^(d * log2e - K) with K = lnS * log2e - log2(c1), for c1 >= 0
+    const bool fold = c1 >= 0.f;
+    // the gradient lines are done with: written back first, ahead of the logits that
+    // pass B of the next row still re-reads from L2
+    const uint64_t pol = l2_evict_first();
+    const float K = fold ? w.lnS * kLog2e - log2f(c1) : 0.f;
     for (int t = 0; t < w.nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
         const int n4 = min(kTileF, w.pt.bn - t * kTileF) >> 2;
+        float4 v[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int j = u * NCT + ct;
+            if (j < n4) v[u] = ld_shared_v4(&S.ring[slot][j * 4]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int j = u * NCT + ct;
             if (j < n4) {
                 const int c0 = w.pt.b0 + t * kTileF + 4 * j;
-                const float4 x = ld_shared_v4(&S.ring[slot][j * 4]);
-                float4 o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS),
-                                       c1 * soft(x.z, w.m, w.lnS), c1 * soft(x.w, w.m, w.lnS));
+                const float4 x = v[u];
+                float4 o;
+                if (fold) {
+                    o = make_float4(ex2(fmaf(x.x - w.m, kLog2e, -K)), ex2(fmaf(x.y - w.m, kLog2e, -K)),
+                                    ex2(fmaf(x.z - w.m, kLog2e, -K)), ex2(fmaf(x.w - w.m, kLog2e, -K)));
+                } else {
+                    o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS),
+                                    c1 * soft(x.z, w.m, w.lnS), c1 * soft(x.w, w.m, w.lnS));
+                }
                 if (w.inwin) {
                     const unsigned d = (unsigned)(w.jl - c0);
                     if (d < 4u) {
@@ -530,11 +581,9 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
                         if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
                     }
                 }
-                st_global_v4(w.rowp + c0, o);
+                st_global_v4_hint(w.rowp + c0, o, pol);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[slot]);
     }
     g += (uint32_t)w.nt;
     if (w.has_ht) {
@@ -656,13 +705,15 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
             wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
             const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+            float4 v[kVec];
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
                 const int j = u * NCT + ct;
-                if (j < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][j * 4]));
+                v[u] = j < n4 ? ld_shared_v4(&S.ring[slot][j * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
+            ms_addv(ms, v);
         }
         g += (uint32_t)cur.nt;
         ms = ms_warp_reduce(ms);
