@@ -10,15 +10,23 @@
 //   * one persistent CTA per SM streams its rows through a ring of 15 KB tiles
 //     (1-D bulk copies, producer warp + 15 consumer warps, as the row engine);
 //   * each consumer warp owns a region of the shared candidate buffer.  A value
-//     enters its warp's region when it is at or above the running threshold T
-//     (the k-th best value kept so far); ties with T are decided by the
-//     composite order (value desc, id asc) at the next selection;
-//   * when a region could overflow, an exact radix select over order-preserving
-//     32-bit keys (-0.0 folded into +0.0; 8-bit digits over the key range
-//     present, warp-private histograms; then over the ids of tied keys) keeps the
-//     best k, spreads them evenly over the regions and raises T;
-//   * at the end of the row the k survivors are ordered by (value desc, id asc)
-//     and written with their probabilities.
+//     enters its warp's region when it is at or above the running threshold T, a
+//     lower bound of the row's k-th largest value (the k-th largest of any subset
+//     of the row is one).  Warps stream independently: there is no barrier per tile;
+//   * a warp whose region could overflow on its next tile, or that sees the
+//     candidate total grow past a few times k, raises a shared flag; every warp
+//     checks it before each tile and while it waits for one, and all of them then
+//     cut the candidates together: a histogram of 10-bit digits of the
+//     order-preserving 32-bit keys (-0.0 folded into +0.0) over the key range
+//     present finds the bin holding the k-th largest key; everything from that
+//     bin's lower edge up is kept (at least k, at most k plus a small slack, a
+//     further digit round narrowing the bin when needed), spread evenly over the
+//     regions, and the lower edge becomes T.  Only when ties at one key exceed the
+//     slack is the cut made exact, the k-th key's ties kept by lowest column;
+//   * at the end of the row the survivors (at most k + 512) are placed into 2048
+//     buckets of the key range in descending order, ranked exactly by
+//     (value desc, id asc) within their bucket, and the first k written with
+//     their probabilities.
 #include "vl_device.cuh"
 #include "vl_internal.h"
 
@@ -30,18 +38,24 @@ namespace {
 constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
-constexpr int kSlotsT = 7;           // ring tiles (105 KB)
-constexpr int RW = 512;              // candidate entries per consumer warp
-constexpr int CB = RW * NCW;         // candidate buffer entries
-constexpr int NPER = RW / 32;        // candidates per lane while compacting
+constexpr int kSlotsT = 7;                 // ring tiles (105 KB)
+constexpr int RW = 512;                    // candidate entries per consumer warp
+constexpr int CB = RW * NCW;               // candidate buffer entries
+constexpr int NPER = RW / 32;              // candidates per lane while cutting
 constexpr int KMAXT = 2048;
-constexpr int DB = 8;                // radix digit bits
-constexpr int NBIN = 1 << DB;
-constexpr int PER_TILE = kTileF / NCW;   // most candidates a warp can add per tile
+constexpr int SLACK = 512;                 // survivors beyond k the final ordering takes
+constexpr int KOUT = KMAXT + SLACK;
+constexpr int DBC = 10;                    // digit bits of one cut round
+constexpr int NBK = 2048;                  // buckets of the final ordering
+constexpr int PER_TILE = kTileF / NCW;     // most candidates a warp can add per tile
+constexpr int LIMIT_MAX = NCW * (RW - PER_TILE - 8);   // survivors that leave each region room for a tile
 constexpr uint32_t kBar = 1;
 
 static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
-static_assert(((KMAXT + NCW - 1) / NCW) + 6 + PER_TILE <= RW, "survivors plus one tile fit a region");
+static_assert(8 + PER_TILE <= RW, "the row's head and tail plus one tile fit an empty region");
+static_assert(KMAXT + KMAXT / 8 <= LIMIT_MAX, "cuts keep at most LIMIT_MAX");
+static_assert((1 << DBC) <= NBK && (NBK & (NBK - 1)) == 0, "histogram sizes");
+static_assert(KOUT <= CB, "the final order is written over the candidate buffer");
 
 __device__ unsigned int g_watchdog;
 
@@ -51,14 +65,16 @@ struct alignas(128) TSmem {
     uint64_t empty[kSlotsT];
     float cval[CB];                  // candidate values, region w = [w * RW, (w + 1) * RW)
     uint32_t cid[CB];
-    uint32_t whist[NCW][NBIN];       // warp-private digit histograms
-    uint32_t hist[NBIN];
-    float okey[KMAXT];               // the k survivors, then in final order
-    uint32_t oid[KMAXT];
+    uint32_t hcnt[NBK];              // digit histogram / bucket sizes
+    uint32_t hpos[NBK];              // bucket starts in descending order
+    uint32_t okey[KOUT];             // survivors in bucket order: key, id
+    uint32_t oid[KOUT];
     uint32_t wtmp[2][NCW];
     uint32_t wcnt[NCW];
     float zred[NCW];
     uint32_t sel[4];
+    uint32_t total;                  // candidates held, counted up as warps append
+    int need;                        // a warp asks for a cut
     int abort;
     uint32_t issued;
 };
@@ -75,9 +91,9 @@ __device__ __forceinline__ float key2f(uint32_t k) {
     return (k & 0x80000000u) ? __uint_as_float(k & 0x7fffffffu) : __uint_as_float(~k);
 }
 
-// composite order: larger value first, then lower id
-__device__ __forceinline__ unsigned long long comp(float v, uint32_t id) {
-    return ((unsigned long long)f2key(v) << 32) | (unsigned long long)(0xffffffffu - id);
+// composite order on (key, id): larger key first, then lower id
+__device__ __forceinline__ unsigned long long comp(uint32_t key, uint32_t id) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - id);
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -117,7 +133,7 @@ __device__ void drain(TSmem& S) {
         wait_parity_drain(&S.full[gt % kSlotsT], (gt / kSlotsT) & 1u);
 }
 
-// ---------------------------------------------------------------- consumer helpers
+// ---------------------------------------------------------------- block-wide helpers (consumer threads)
 
 // Append `keep` lanes' (value, id) to this warp's region; cnt is the warp's count.
 __device__ __forceinline__ void wappend(TSmem& S, int cw, uint32_t& cnt, bool keep, float v, uint32_t id) {
@@ -130,16 +146,9 @@ __device__ __forceinline__ void wappend(TSmem& S, int cw, uint32_t& cnt, bool ke
     cnt += (uint32_t)__popc(bal);
 }
 
-// The K-th largest of f[j] over the slots with bit j of vmask set, 1 <= K <= count.
-// Returns v*; *above = #{f > v*}, *eq = #{f == v*}.  Exact MSD radix select, 8-bit
-// digits over the range [min, max] present, warp-private histograms.
-__device__ __forceinline__ uint32_t select_kth_largest(const uint32_t (&f)[NPER], uint32_t vmask, uint32_t K,
-                                                       TSmem& S, int ct, uint32_t* above, uint32_t* eq) {
+// Block-wide min and max of u32s.  The caller separates the next use of S.wtmp by a barrier.
+__device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, TSmem& S, int ct) {
     const int cw = ct >> 5, lane = ct & 31;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll
-    for (int j = 0; j < NPER; ++j)
-        if (vmask >> j & 1u) { lo = min(lo, f[j]); hi = max(hi, f[j]); }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
@@ -151,77 +160,86 @@ __device__ __forceinline__ uint32_t select_kth_largest(const uint32_t (&f)[NPER]
     hi = S.wtmp[1][0];
 #pragma unroll
     for (int w = 1; w < NCW; ++w) { lo = min(lo, S.wtmp[0][w]); hi = max(hi, S.wtmp[1][w]); }
+}
+
+// Sum of v over the consumer threads with a higher index.  The caller separates the
+// next use of S.wtmp by a barrier.
+__device__ __forceinline__ uint32_t block_above(uint32_t v, TSmem& S, int ct) {
+    const int cw = ct >> 5, lane = ct & 31;
+    uint32_t suf = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf += t;
+    }
+    if (lane == 0) S.wtmp[0][cw] = suf;
+    named_sync(kBar, NCT);
+    uint32_t a = suf - v;
+    for (int w = cw + 1; w < NCW; ++w) a += S.wtmp[0][w];
+    return a;
+}
+
+struct Cut {
+    uint32_t tk;     // keep the keys >= tk
+    uint32_t ge;     // keys >= tk
+    uint32_t gt;     // keys > tk (exact cuts)
+    bool exact;      // tk is the K-th largest key itself
+};
+
+// Over the keys f[j] of the slots with bit j of vmask set (K <= their count): a key
+// tk with K <= #(f >= tk).  MSD digit rounds of DBC bits over the range [min, max]
+// present narrow the bin holding the K-th largest key until #(f >= its lower edge)
+// <= limit, or until the bin is one key (then tk is the K-th largest key, exact).
+__device__ Cut select_cut(const uint32_t (&f)[NPER], uint32_t vmask, uint32_t K, uint32_t limit, TSmem& S, int ct) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j)
+        if (vmask >> j & 1u) { lo = min(lo, f[j]); hi = max(hi, f[j]); }
+    block_minmax(lo, hi, S, ct);
     const uint32_t R = hi - lo;
     int shift = R ? 32 - __clz(R) : 0;
-    uint32_t prefix = 0, rem = K, abv = 0, eqc = 0;
-    int bits = 0;
-    do {
-        bits = shift < DB ? shift : DB;
+    uint32_t prefix = 0, rem = K, abv = 0;
+    for (;;) {
+        const int bits = shift < DBC ? shift : DBC;
         shift -= bits;
-        const uint32_t dmask = (1u << bits) - 1u;
-        uint32_t* wh = S.whist[cw];
-#pragma unroll
-        for (int i = lane; i < NBIN; i += 32) wh[i] = 0u;
-        __syncwarp();
+        const int nb = 1 << bits;
+        for (int i = ct; i < nb; i += NCT) S.hcnt[i] = 0u;
+        named_sync(kBar, NCT);
 #pragma unroll
         for (int j = 0; j < NPER; ++j) {
             if (vmask >> j & 1u) {
                 const uint32_t u = f[j] - lo;
                 const uint32_t top = (shift + bits >= 32) ? 0u : (u >> (shift + bits));
-                if (top == prefix) atomicAdd(&wh[(u >> shift) & dmask], 1u);
+                if (top == prefix) atomicAdd(&S.hcnt[(u >> shift) & (uint32_t)(nb - 1)], 1u);
             }
         }
         named_sync(kBar, NCT);
-        if (ct < NBIN) {
-            uint32_t s = 0;
-#pragma unroll
-            for (int w = 0; w < NCW; ++w) s += S.whist[w][ct];
-            S.hist[ct] = s;
+        // thread ct owns bins [c0, c1); the bin holding the K-th largest is found from the top
+        const int per = (nb + NCT - 1) / NCT;
+        const int c0 = min(nb, ct * per), c1 = min(nb, c0 + per);
+        uint32_t loc = 0;
+        for (int i = c0; i < c1; ++i) loc += S.hcnt[i];
+        uint32_t a = block_above(loc, S, ct);
+        for (int i = c1 - 1; i >= c0; --i) {
+            const uint32_t c = S.hcnt[i];
+            if (a < rem && rem <= a + c) { S.sel[0] = (uint32_t)i; S.sel[1] = a; S.sel[2] = c; }
+            a += c;
         }
         named_sync(kBar, NCT);
-        if (cw == 0) {
-            // suffix sums over the bins, lane l owns bins [8 l, 8 l + 8)
-            uint32_t hs[8];
-            uint32_t loc = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { hs[i] = S.hist[8 * lane + i]; loc += hs[i]; }
-            uint32_t suf = loc;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t v = __shfl_down_sync(0xffffffffu, suf, off);
-                if (lane + off < 32) suf += v;
-            }
-            uint32_t a = suf - loc;     // entries in bins above this lane's
-#pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                if (a < rem && rem <= a + hs[i]) {
-                    S.sel[0] = (uint32_t)(8 * lane + i);
-                    S.sel[1] = a;
-                    S.sel[2] = hs[i];
-                }
-                a += hs[i];
-            }
-        }
-        named_sync(kBar, NCT);
-        const uint32_t bin = S.sel[0], ab = S.sel[1], cnt = S.sel[2];
-        rem -= ab;
+        const uint32_t b = S.sel[0], ab = S.sel[1], cb = S.sel[2];
         abv += ab;
-        prefix = (prefix << bits) | bin;
-        eqc = cnt;
-        if (shift > 0) named_sync(kBar, NCT);   // S.sel and the histograms are reused
-    } while (shift > 0);
-    *above = abv;
-    *eq = eqc;
-    return lo + prefix;
+        rem -= ab;
+        prefix = (prefix << bits) | b;
+        const uint32_t ge = abv + cb;
+        if (shift == 0) return Cut{lo + prefix, ge, abv, true};
+        if (ge <= limit) return Cut{lo + (prefix << shift), ge, abv, false};
+        named_sync(kBar, NCT);   // S.sel and S.hcnt are reused
+    }
 }
 
-// Keep exactly the best K candidates (value desc, id asc) of all regions (all of them
-// when there are at most K) and spread them evenly over the regions, at most
-// ceil(K / NCW) each.  `tot` is the number of candidates.  Returns true and the K-th
-// best value in *T when a selection was made: later columns are admitted above it.
-__device__ __forceinline__ bool compact(TSmem& S, uint32_t K, uint32_t tot, int ct, uint32_t& cnt, float* T) {
-    const int cw = ct >> 5, lane = ct & 31;
-    uint32_t key[NPER], id[NPER];
+// This warp's candidates into registers: key[j], id[j] for slot lane + 32 j < cnt.
+__device__ __forceinline__ uint32_t load_region(const TSmem& S, int cw, int lane, uint32_t cnt, uint32_t (&key)[NPER],
+                                                uint32_t (&id)[NPER]) {
     uint32_t vmask = 0;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
@@ -234,32 +252,55 @@ __device__ __forceinline__ bool compact(TSmem& S, uint32_t K, uint32_t tot, int 
             vmask |= 1u << j;
         }
     }
-    const bool sel = tot > K;
-    uint32_t Tk = 0u, idmax = 0xffffffffu;
-    if (sel) {
-        uint32_t above, eq;
-        Tk = select_kth_largest(key, vmask, K, S, ct, &above, &eq);
-        const uint32_t need = K - above;
-        if (eq > need) {
-            uint32_t nid[NPER];
-            uint32_t emask = 0;
+    return vmask;
+}
+
+// Which loaded candidates survive when tot > K: keys >= a cut that keeps at most `limit`
+// (and at least K); when ties at the exact K-th key exceed that, exactly K, the tied
+// keys by lowest id.  *tk is the cut key.
+__device__ uint32_t choose(const uint32_t (&key)[NPER], const uint32_t (&id)[NPER], uint32_t vmask, uint32_t K,
+                           uint32_t limit, TSmem& S, int ct, uint32_t* tk) {
+    const Cut c = select_cut(key, vmask, K, limit, S, ct);
+    *tk = c.tk;
+    uint32_t idmax = 0xffffffffu;
+    if (c.exact && c.ge > limit) {
+        uint32_t nid[NPER];
+        uint32_t emask = 0;
 #pragma unroll
-            for (int j = 0; j < NPER; ++j) {
-                nid[j] = ~id[j];
-                if ((vmask >> j & 1u) && key[j] == Tk) emask |= 1u << j;
-            }
-            named_sync(kBar, NCT);
-            uint32_t a2, e2;
-            idmax = ~select_kth_largest(nid, emask, need, S, ct, &a2, &e2);
+        for (int j = 0; j < NPER; ++j) {
+            nid[j] = ~id[j];
+            if ((vmask >> j & 1u) && key[j] == c.tk) emask |= 1u << j;
         }
+        named_sync(kBar, NCT);
+        const uint32_t need = K - c.gt;
+        const Cut ci = select_cut(nid, emask, need, need, S, ct);   // ids are distinct: exactly `need`
+        idmax = ~ci.tk;
     }
-    uint32_t keep = 0, kept = 0;
+    uint32_t keep = 0;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
-        const bool kj = (vmask >> j & 1u) && (!sel || key[j] > Tk || (key[j] == Tk && id[j] <= idmax));
+        const bool kj = (vmask >> j & 1u) && (key[j] > c.tk || (key[j] == c.tk && id[j] <= idmax));
         keep |= (uint32_t)kj << j;
-        kept += (uint32_t)__popc(__ballot_sync(0xffffffffu, kj));
     }
+    return keep;
+}
+
+// All consumer warps: cut the candidates of all regions (when there are more than K),
+// spread the survivors evenly over the regions and raise T.  cnt: this warp's count.
+__device__ __noinline__ void compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t& cnt,
+                                     float& T) {
+    const int cw = ct >> 5, lane = ct & 31;
+    uint32_t key[NPER], id[NPER];
+    const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
+    uint32_t keep = vmask;
+    if (tot > K) {
+        uint32_t tk;
+        keep = choose(key, id, vmask, K, limit, S, ct, &tk);
+        T = key2f(tk);
+    }
+    uint32_t kept = 0;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) kept += (uint32_t)__popc(__ballot_sync(0xffffffffu, keep >> j & 1u));
     named_sync(kBar, NCT);                 // every region has been read into registers
     if (lane == 0) S.wcnt[cw] = kept;
     named_sync(kBar, NCT);
@@ -285,9 +326,110 @@ __device__ __forceinline__ bool compact(TSmem& S, uint32_t K, uint32_t tot, int 
     }
     const int left = (int)total - cw * (int)per;
     cnt = left <= 0 ? 0u : (left < (int)per ? (uint32_t)left : per);
-    named_sync(kBar, NCT);                 // regions rewritten, S.wcnt read
-    if (sel) *T = key2f(Tk);
-    return sel;
+    if (ct == 0) { S.total = total; S.need = 0; }
+    named_sync(kBar, NCT);                 // regions rewritten, S.wcnt read, flag lowered
+}
+
+// Entry of every warp into a collective step.  Returns how many warps had finished the
+// row; unless all had, the candidates are cut (compact) before returning.
+__device__ __forceinline__ uint32_t collective(TSmem& S, uint32_t K, uint32_t limit, int ct, uint32_t& cnt, float& T,
+                                               bool fin) {
+    const int cw = ct >> 5, lane = ct & 31;
+    if (lane == 0) S.wcnt[cw] = cnt;
+    const uint32_t nfin = named_sync_popc(kBar, NCT, fin && lane == 0);
+    if (nfin == (uint32_t)NCW) return nfin;
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
+    named_sync(kBar, NCT);                 // S.wcnt is rewritten by compact
+    compact(S, K, limit, tot, ct, cnt, T);
+    return nfin;
+}
+
+// The end of a row, all warps: at most K + SLACK survivors, ordered by (value desc, id asc)
+// through 2048 buckets of the key range, the first K written with their probabilities.
+__device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t cnt, long long r, uint32_t* ids,
+                                        float* probs) {
+    const int cw = ct >> 5, lane = ct & 31;
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
+    uint32_t key[NPER], id[NPER];
+    const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
+    uint32_t keep = vmask;
+    if (tot > K + (uint32_t)SLACK) {
+        uint32_t tk;
+        keep = choose(key, id, vmask, K, K + (uint32_t)SLACK, S, ct, &tk);
+        named_sync(kBar, NCT);             // S.sel, S.hcnt and S.wtmp are reused
+    }
+    // ---- buckets: an 11-bit window of (key - lo), higher buckets first
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j)
+        if (keep >> j & 1u) { lo = min(lo, key[j]); hi = max(hi, key[j]); }
+    block_minmax(lo, hi, S, ct);
+    const uint32_t R = hi - lo;
+    const int nbits = R ? 32 - __clz(R) : 0;
+    const int s2 = nbits > 11 ? nbits - 11 : 0;
+    for (int i = ct; i < NBK; i += NCT) S.hcnt[i] = 0u;
+    named_sync(kBar, NCT);
+#pragma unroll
+    for (int j = 0; j < NPER; ++j)
+        if (keep >> j & 1u) atomicAdd(&S.hcnt[(key[j] - lo) >> s2], 1u);
+    named_sync(kBar, NCT);
+    {
+        constexpr int per = (NBK + NCT - 1) / NCT;
+        const int c0 = min(NBK, ct * per), c1 = min(NBK, c0 + per);
+        uint32_t loc = 0;
+        for (int i = c0; i < c1; ++i) loc += S.hcnt[i];
+        uint32_t a = block_above(loc, S, ct);
+        for (int i = c1 - 1; i >= c0; --i) {
+            S.hpos[i] = a;
+            a += S.hcnt[i];
+        }
+    }
+    named_sync(kBar, NCT);
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        if (keep >> j & 1u) {
+            const uint32_t p = atomicAdd(&S.hpos[(key[j] - lo) >> s2], 1u);
+            S.okey[p] = key[j];
+            S.oid[p] = id[j];
+        }
+    }
+    named_sync(kBar, NCT);
+    // ---- exact rank: the bucket's start plus the members ahead in (key desc, id asc)
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        if (keep >> j & 1u) {
+            const uint32_t bk = (key[j] - lo) >> s2;
+            const uint32_t end = S.hpos[bk], beg = end - S.hcnt[bk];
+            const unsigned long long me = comp(key[j], id[j]);
+            uint32_t rank = beg;
+            for (uint32_t i = beg; i < end; ++i) rank += comp(S.okey[i], S.oid[i]) > me ? 1u : 0u;
+            if (rank < K) {
+                S.cval[rank] = key2f(key[j]);
+                S.cid[rank] = id[j];
+            }
+        }
+    }
+    named_sync(kBar, NCT);
+    // ---- probabilities renormalised over the k, summed in rank order
+    const float v0 = S.cval[0];
+    float part = 0.f;
+    for (uint32_t q = (uint32_t)ct; q < K; q += NCT) part += expf(S.cval[q] - v0);
+    part = warp_sum(part);
+    if (lane == 0) S.zred[cw] = part;
+    named_sync(kBar, NCT);
+    float Z = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) Z += S.zred[w];
+    for (uint32_t q = (uint32_t)ct; q < K; q += NCT) {
+        ids[r * K + q] = S.cid[q];
+        probs[r * K + q] = expf(S.cval[q] - v0) / Z;
+    }
+    if (ct == 0) { S.total = 0; S.need = 0; }
+    named_sync(kBar, NCT);   // the regions, S.zred and S.total are reused by the next row
 }
 
 // ---------------------------------------------------------------- consumer
@@ -296,6 +438,10 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
                          uint32_t* ids, float* probs, TSmem& S) {
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
+    const uint32_t K = (uint32_t)k;
+    const uint32_t limit = min((uint32_t)LIMIT_MAX, K + max(K / 8u, 64u));   // survivors of a cut
+    const uint32_t trig = max(4u * K, 1024u);                               // total that asks for a cut
+    volatile int* need = &S.need;
     uint32_t g = 0;
     for (long long r = ls + (long long)blockIdx.x; r < le; r += gridDim.x) {
         const float* rowp = x + r * ld;
@@ -307,8 +453,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         const int nt = (bt + kTileF - 1) / kTileF;
 
         uint32_t cnt = 0;          // this warp's candidates (same in every lane)
-        bool armed = false;        // a threshold exists once k candidates were kept
-        float T = 0.f;
+        float T = -INFINITY;       // admission threshold: everything until the first cut
         // head and tail columns (at most 3 + 3) go to warp 0 unconditionally
         if (cw == 0) {
             bool keep = false;
@@ -319,8 +464,35 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             wappend(S, cw, cnt, keep, v, id);
         }
         for (int t = 0; t < nt; ++t) {
-            const uint32_t gt = g + (uint32_t)t, slot = gt % kSlotsT;
-            wait_parity<false>(&S.full[slot], (gt / kSlotsT) & 1u, &S.abort, &g_watchdog);
+            const uint32_t gt = g + (uint32_t)t, slot = gt % kSlotsT, par = (gt / kSlotsT) & 1u;
+            // a cut first when another warp asks for one or this region has no room for a tile
+            if (__shfl_sync(0xffffffffu, *need, 0) || cnt + PER_TILE > (uint32_t)RW) {
+                if (lane == 0) *need = 1;
+                collective(S, K, limit, ct, cnt, T, false);
+            }
+            // the tile; a cut asked for by another warp is joined while waiting
+            {
+                const uint32_t fb = smem_u32(&S.full[slot]);
+                long long w0 = 0;
+                for (uint32_t it = 0;; ++it) {
+                    if (__all_sync(0xffffffffu, mbar_try_wait(fb, par))) break;
+                    if (__shfl_sync(0xffffffffu, *need, 0)) {
+                        collective(S, K, limit, ct, cnt, T, false);
+                        continue;
+                    }
+                    if ((it & 255u) == 255u) {
+                        if (S.abort) break;
+                        const long long now = clock64();
+                        if (w0 == 0) {
+                            w0 = now;
+                        } else if (now - w0 > kWaitTimeoutCycles) {
+                            S.abort = 1;
+                            atomicOr(&g_watchdog, 1u);
+                            break;
+                        }
+                    }
+                }
+            }
             const int n4 = min(kTileF, bt - t * kTileF) >> 2;
             float4 v[kVec];
 #pragma unroll
@@ -330,118 +502,31 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
+            const uint32_t before = cnt;
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
                 const int j = u * NCT + ct;
                 const bool active = j < n4;
                 // most float4s hold nothing at or above the threshold: one vote per warp
-                const bool any = active && (!armed || fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T);
+                const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
                 if (__any_sync(0xffffffffu, any)) {
                     const uint32_t c0 = (uint32_t)(h + t * kTileF + 4 * j);
-                    wappend(S, cw, cnt, any && (!armed || v[u].x >= T), v[u].x, c0);
-                    wappend(S, cw, cnt, any && (!armed || v[u].y >= T), v[u].y, c0 + 1);
-                    wappend(S, cw, cnt, any && (!armed || v[u].z >= T), v[u].z, c0 + 2);
-                    wappend(S, cw, cnt, any && (!armed || v[u].w >= T), v[u].w, c0 + 3);
+                    wappend(S, cw, cnt, any && v[u].x >= T, v[u].x, c0);
+                    wappend(S, cw, cnt, any && v[u].y >= T, v[u].y, c0 + 1);
+                    wappend(S, cw, cnt, any && v[u].z >= T, v[u].z, c0 + 2);
+                    wappend(S, cw, cnt, any && v[u].w >= T, v[u].w, c0 + 3);
                 }
             }
-            // compact when some region could overflow on the next tile
-            if (t + 1 < nt) {
-                const uint32_t full = named_sync_popc(kBar, NCT, lane == 0 && cnt + PER_TILE > (uint32_t)RW);
-                if (full) {
-                    if (lane == 0) S.wcnt[cw] = cnt;
-                    named_sync(kBar, NCT);
-                    uint32_t tot = 0;
-#pragma unroll
-                    for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
-                    named_sync(kBar, NCT);
-                    armed |= compact(S, (uint32_t)k, tot, ct, cnt, &T);
-                }
+            // many candidates overall: ask for a cut, which raises T
+            if (lane == 0 && cnt != before) {
+                const uint32_t now = atomicAdd(&S.total, cnt - before) + (cnt - before);
+                if (now > trig) *need = 1;
             }
         }
         g += (uint32_t)nt;
-
-        // ---- exactly k survivors, gathered in one array
-        if (lane == 0) S.wcnt[cw] = cnt;
-        named_sync(kBar, NCT);
-        uint32_t tot = 0;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
-        named_sync(kBar, NCT);
-        if (tot > (uint32_t)k) compact(S, (uint32_t)k, tot, ct, cnt, &T);
-        if (lane == 0) S.wcnt[cw] = cnt;
-        named_sync(kBar, NCT);
-        uint32_t base = 0;
-#pragma unroll
-        for (int w = 0; w < cw; ++w) base += S.wcnt[w];
-        for (uint32_t i = (uint32_t)lane; i < cnt; i += 32) {
-            S.okey[base + i] = S.cval[cw * RW + i];
-            S.oid[base + i] = S.cid[cw * RW + i];
+        while (collective(S, K, limit, ct, cnt, T, true) != (uint32_t)NCW) {
         }
-        named_sync(kBar, NCT);
-
-        // ---- order the k survivors by (value desc, id asc)
-        const uint32_t K = (uint32_t)k;
-        if (K <= (uint32_t)NCT) {
-            // rank of each survivor among all k by the composite key, built once
-            unsigned long long* ck = reinterpret_cast<unsigned long long*>(S.cval);
-            const bool mine = (uint32_t)ct < K;
-            float mv = 0.f;
-            uint32_t mi = 0;
-            unsigned long long mc = 0;
-            if (mine) { mv = S.okey[ct]; mi = S.oid[ct]; mc = comp(mv, mi); ck[ct] = mc; }
-            named_sync(kBar, NCT);
-            if (mine) {
-                uint32_t p0 = 0, p1 = 0, p2 = 0, p3 = 0, j = 0;
-                for (; j + 4 <= K; j += 4) {
-                    p0 += ck[j] > mc;
-                    p1 += ck[j + 1] > mc;
-                    p2 += ck[j + 2] > mc;
-                    p3 += ck[j + 3] > mc;
-                }
-                for (; j < K; ++j) p0 += ck[j] > mc;
-                const uint32_t pos = (p0 + p1) + (p2 + p3);
-                S.okey[pos] = mv;      // every thread read its own entry before the barrier
-                S.oid[pos] = mi;
-            }
-            named_sync(kBar, NCT);
-        } else {
-            uint32_t Kp = 1;
-            while (Kp < K) Kp <<= 1;
-            for (uint32_t i = K + (uint32_t)ct; i < Kp; i += NCT) { S.okey[i] = -INFINITY; S.oid[i] = 0xffffffffu; }
-            named_sync(kBar, NCT);
-            for (uint32_t size = 2; size <= Kp; size <<= 1) {
-                for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-                    for (uint32_t i = (uint32_t)ct; i < Kp / 2; i += NCT) {
-                        const uint32_t a = 2 * stride * (i / stride) + (i % stride), b = a + stride;
-                        const bool down = (a & size) == 0u;
-                        const unsigned long long ca = comp(S.okey[a], S.oid[a]), cb = comp(S.okey[b], S.oid[b]);
-                        if (down ? (ca < cb) : (ca > cb)) {
-                            const float tv = S.okey[a];
-                            const uint32_t ti = S.oid[a];
-                            S.okey[a] = S.okey[b]; S.oid[a] = S.oid[b];
-                            S.okey[b] = tv; S.oid[b] = ti;
-                        }
-                    }
-                    named_sync(kBar, NCT);
-                }
-            }
-        }
-
-        // ---- probabilities renormalised over the k, summed in rank order
-        const float v0 = S.okey[0];
-        float part = 0.f;
-        for (uint32_t q = (uint32_t)ct; q < K; q += NCT) part += expf(S.okey[q] - v0);
-        part = warp_sum(part);
-        if (lane == 0) S.zred[cw] = part;
-        named_sync(kBar, NCT);
-        float Z = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) Z += S.zred[w];
-        for (uint32_t q = (uint32_t)ct; q < K; q += NCT) {
-            ids[r * k + q] = S.oid[q];
-            probs[r * k + q] = expf(S.okey[q] - v0) / Z;
-        }
-        named_sync(kBar, NCT);   // okey, zred and the regions are reused by the next row
+        finish_row(S, K, ct, cnt, r, ids, probs);
     }
 }
 
@@ -457,6 +542,8 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
         }
         S.abort = 0;
         S.issued = 0;
+        S.total = 0;
+        S.need = 0;
         fence_mbar_init_cluster();
     }
     __syncthreads();

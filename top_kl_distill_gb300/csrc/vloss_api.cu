@@ -144,23 +144,57 @@ __global__ void acc_add_scalar_kernel(float* a, const float* b, long long n) {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) a[i] = a[i] + b[i];
 }
 
-// mean of loss[ls, le), summed in double in a fixed order.  Launched as a
-// programmatic dependent of the loss kernel: its launch overlaps that kernel,
-// griddepcontrol.wait holds it until the losses are in memory.
+// Error-free sum of two floats (Knuth's TwoSum): a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// (hi, lo) += (h2, l2) for unevaluated float pairs (double-float addition).
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float h2, float l2) {
+    float s, e;
+    two_sum(hi, h2, s, e);
+    e += lo + l2;
+    two_sum(s, e, hi, lo);
+}
+
+// mean of loss[ls, le), accumulated as float pairs (about 48 significant bits) in a
+// fixed order, so the result does not depend on the launch and needs no FP64 unit.
+// Launched as a programmatic dependent of the loss kernel: its launch overlaps that
+// kernel, griddepcontrol.wait holds it until the losses are in memory.
 __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ loss, long long ls, long long le,
                                                     float* __restrict__ mean) {
     pdl_wait_primary();
-    __shared__ double red[32];
-    double acc = 0.0;
-    for (long long i = ls + threadIdx.x; i < le; i += blockDim.x) acc += (double)loss[i];
+    __shared__ float2 red[32];
+    float hi = 0.f, lo = 0.f;
+    for (long long i = ls + threadIdx.x; i < le; i += blockDim.x) ff_add(hi, lo, loss[i], 0.f);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    for (int off = 16; off > 0; off >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+        ff_add(hi, lo, h2, l2);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float2(hi, lo);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double s = 0.0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-        *mean = le > ls ? (float)(s / (double)(le - ls)) : 0.0f;
+    if (threadIdx.x < 32) {
+        const int nw = (int)(blockDim.x >> 5);
+        float2 v = (int)threadIdx.x < nw ? red[threadIdx.x] : make_float2(0.f, 0.f);
+        hi = v.x;
+        lo = v.y;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+            ff_add(hi, lo, h2, l2);
+        }
+        if (threadIdx.x == 0) {
+            // (hi + lo) / n: the quotient of the pair, one correction step
+            const float n = (float)(le - ls);
+            float q = hi / n, pe;
+            const float p = q * n;
+            pe = fmaf(q, n, -p);                     // q * n = p + pe exactly
+            q += ((hi - p) - pe + lo) / n;
+            *mean = le > ls ? q : 0.0f;
+        }
     }
 }
 
