@@ -45,7 +45,8 @@ constexpr int NPER = RW / 32;              // candidates per lane while cutting
 constexpr int KMAXT = 2048;
 constexpr int SLACK = 512;                 // survivors beyond k the final ordering takes
 constexpr int KOUT = KMAXT + SLACK;
-constexpr int DBC = 10;                    // digit bits of one cut round
+constexpr int DBC = 10;                    // digit bits of one exact cut round
+constexpr int NBC = 1024;                  // linear bins of a cut
 constexpr int NBK = 2048;                  // buckets of the final ordering
 constexpr int PER_TILE = kTileF / NCW;     // most candidates a warp can add per tile
 constexpr int LIMIT_MAX = NCW * (RW - PER_TILE - 8);   // survivors that leave each region room for a tile
@@ -285,6 +286,56 @@ __device__ uint32_t choose(const uint32_t (&key)[NPER], const uint32_t (&id)[NPE
     return keep;
 }
 
+// A cut over linear bins of the value range: the loaded candidates (keys, vmask) fall into
+// NBC equal bins of [min, max]; the bins from the one holding the K-th largest value up
+// are kept when they hold at most `limit` candidates.  The bin index is a monotone
+// function of the value, so the kept set holds the K largest.  Returns false (nothing
+// decided) when the range is empty or not finite, or the boundary bin is too crowded.
+// S.hcnt[0, NBC) must be zero on entry and is zero again on return.
+__device__ bool linear_cut(const uint32_t (&key)[NPER], uint32_t vmask, uint32_t K, uint32_t limit, TSmem& S, int ct,
+                           uint32_t* keep) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j)
+        if (vmask >> j & 1u) { lo = min(lo, key[j]); hi = max(hi, key[j]); }
+    block_minmax(lo, hi, S, ct);
+    const float vmin = key2f(lo), vmax = key2f(hi);
+    const float range = vmax - vmin;
+    if (!(range > 0.f) || !(range < INFINITY)) return false;    // every thread sees the same
+    const float scale = (float)NBC / range;
+    uint32_t bin[NPER];
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) {
+        bin[j] = min((uint32_t)(NBC - 1), (uint32_t)((key2f(key[j]) - vmin) * scale));
+        if (vmask >> j & 1u) atomicAdd(&S.hcnt[bin[j]], 1u);
+    }
+    named_sync(kBar, NCT);
+    constexpr int per = (NBC + NCT - 1) / NCT;
+    const int c0 = min(NBC, ct * per), c1 = min(NBC, c0 + per);
+    uint32_t hc[per];
+    uint32_t loc = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+        hc[i] = c0 + i < c1 ? S.hcnt[c0 + i] : 0u;
+        loc += hc[i];
+        if (c0 + i < c1) S.hcnt[c0 + i] = 0u;            // zero again for the next cut
+    }
+    uint32_t a = block_above(loc, S, ct);
+#pragma unroll
+    for (int i = per - 1; i >= 0; --i) {
+        if (a < K && K <= a + hc[i]) { S.sel[0] = (uint32_t)(c0 + i); S.sel[1] = a + hc[i]; }
+        a += hc[i];
+    }
+    named_sync(kBar, NCT);
+    const uint32_t b = S.sel[0], ge = S.sel[1];
+    if (ge > limit) return false;
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < NPER; ++j) m |= (uint32_t)((vmask >> j & 1u) && bin[j] >= b) << j;
+    *keep = m;
+    return true;
+}
+
 // All consumer warps: cut the candidates of all regions (when there are more than K),
 // spread the survivors evenly over the regions and raise T.  cnt: this warp's count.
 __device__ __noinline__ void compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t& cnt,
@@ -294,40 +345,53 @@ __device__ __noinline__ void compact(TSmem& S, uint32_t K, uint32_t limit, uint3
     const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
     uint32_t keep = vmask;
     if (tot > K) {
-        uint32_t tk;
-        keep = choose(key, id, vmask, K, limit, S, ct, &tk);
-        T = key2f(tk);
+        if (!linear_cut(key, vmask, K, limit, S, ct, &keep)) {
+            named_sync(kBar, NCT);           // S.wtmp and S.sel are reused
+            uint32_t tk;
+            keep = choose(key, id, vmask, K, limit, S, ct, &tk);
+            named_sync(kBar, NCT);
+            for (int i = ct; i < NBC; i += NCT) S.hcnt[i] = 0u;
+        }
     }
-    uint32_t kept = 0;
+    // the smallest kept key: the new threshold (the K-th largest of the row is at least it)
+    uint32_t kept = 0, kmin = 0xffffffffu;
 #pragma unroll
-    for (int j = 0; j < NPER; ++j) kept += (uint32_t)__popc(__ballot_sync(0xffffffffu, keep >> j & 1u));
+    for (int j = 0; j < NPER; ++j) {
+        const bool kj = keep >> j & 1u;
+        kept += (uint32_t)__popc(__ballot_sync(0xffffffffu, kj));
+        if (kj) kmin = min(kmin, key[j]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
     named_sync(kBar, NCT);                 // every region has been read into registers
-    if (lane == 0) S.wcnt[cw] = kept;
+    if (lane == 0) { S.wcnt[cw] = kept; S.wtmp[1][cw] = kmin; }
     named_sync(kBar, NCT);
     uint32_t base = 0, total = 0;
+    kmin = 0xffffffffu;
 #pragma unroll
     for (int w = 0; w < NCW; ++w) {
         const uint32_t c = S.wcnt[w];
         base += w < cw ? c : 0u;
         total += c;
+        kmin = min(kmin, S.wtmp[1][w]);
     }
-    const uint32_t per = (total + NCW - 1) / NCW;
+    if (tot > K) T = key2f(kmin);
+    // survivor i goes to region i % NCW, entry i / NCW
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const bool kj = keep >> j & 1u;
         const uint32_t bal = __ballot_sync(0xffffffffu, kj);
         if (kj) {
             const uint32_t i = base + (uint32_t)__popc(bal & lanemask_lt());
-            const uint32_t slot = (i / per) * RW + i % per;
+            const uint32_t slot = (i % (uint32_t)NCW) * RW + i / (uint32_t)NCW;
             S.cval[slot] = key2f(key[j]);   // -0.0 comes back as +0.0: same rank, same probability
             S.cid[slot] = id[j];
         }
         base += (uint32_t)__popc(bal);
     }
-    const int left = (int)total - cw * (int)per;
-    cnt = left <= 0 ? 0u : (left < (int)per ? (uint32_t)left : per);
+    cnt = (total + (uint32_t)(NCW - 1 - cw)) / (uint32_t)NCW;
     if (ct == 0) { S.total = total; S.need = 0; }
-    named_sync(kBar, NCT);                 // regions rewritten, S.wcnt read, flag lowered
+    named_sync(kBar, NCT);                 // regions rewritten, S.wcnt and S.wtmp read, flag lowered
 }
 
 // Entry of every warp into a collective step.  Returns how many warps had finished the
@@ -358,24 +422,34 @@ __device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t c
     const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
     uint32_t keep = vmask;
     if (tot > K + (uint32_t)SLACK) {
-        uint32_t tk;
-        keep = choose(key, id, vmask, K, K + (uint32_t)SLACK, S, ct, &tk);
+        const bool done = linear_cut(key, vmask, K, K + (uint32_t)SLACK, S, ct, &keep);
         named_sync(kBar, NCT);             // S.sel, S.hcnt and S.wtmp are reused
+        if (!done) {
+            uint32_t tk;
+            keep = choose(key, id, vmask, K, K + (uint32_t)SLACK, S, ct, &tk);
+            named_sync(kBar, NCT);
+        }
     }
-    // ---- buckets: an 11-bit window of (key - lo), higher buckets first
+    // ---- buckets: NBK equal bins of the value range when it is finite and not empty,
+    //      else an 11-bit window of (key - lo); higher buckets first
     uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
     for (int j = 0; j < NPER; ++j)
         if (keep >> j & 1u) { lo = min(lo, key[j]); hi = max(hi, key[j]); }
+    for (int i = ct; i < NBK; i += NCT) S.hcnt[i] = 0u;
     block_minmax(lo, hi, S, ct);
+    const float vmin = key2f(lo), range = key2f(hi) - vmin;
+    const bool lin = range > 0.f && range < INFINITY;
+    const float scale = lin ? (float)NBK / range : 0.f;
     const uint32_t R = hi - lo;
     const int nbits = R ? 32 - __clz(R) : 0;
     const int s2 = nbits > 11 ? nbits - 11 : 0;
-    for (int i = ct; i < NBK; i += NCT) S.hcnt[i] = 0u;
-    named_sync(kBar, NCT);
+    auto bucket = [&](uint32_t kk) -> uint32_t {
+        return lin ? min((uint32_t)(NBK - 1), (uint32_t)((key2f(kk) - vmin) * scale)) : (kk - lo) >> s2;
+    };
 #pragma unroll
     for (int j = 0; j < NPER; ++j)
-        if (keep >> j & 1u) atomicAdd(&S.hcnt[(key[j] - lo) >> s2], 1u);
+        if (keep >> j & 1u) atomicAdd(&S.hcnt[bucket(key[j])], 1u);
     named_sync(kBar, NCT);
     {
         constexpr int per = (NBK + NCT - 1) / NCT;
@@ -392,7 +466,7 @@ __device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t c
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         if (keep >> j & 1u) {
-            const uint32_t p = atomicAdd(&S.hpos[(key[j] - lo) >> s2], 1u);
+            const uint32_t p = atomicAdd(&S.hpos[bucket(key[j])], 1u);
             S.okey[p] = key[j];
             S.oid[p] = id[j];
         }
@@ -402,7 +476,7 @@ __device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t c
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         if (keep >> j & 1u) {
-            const uint32_t bk = (key[j] - lo) >> s2;
+            const uint32_t bk = bucket(key[j]);
             const uint32_t end = S.hpos[bk], beg = end - S.hcnt[bk];
             const unsigned long long me = comp(key[j], id[j]);
             uint32_t rank = beg;
@@ -428,6 +502,7 @@ __device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t c
         ids[r * K + q] = S.cid[q];
         probs[r * K + q] = expf(S.cval[q] - v0) / Z;
     }
+    for (int i = ct; i < NBC; i += NCT) S.hcnt[i] = 0u;
     if (ct == 0) { S.total = 0; S.need = 0; }
     named_sync(kBar, NCT);   // the regions, S.zred and S.total are reused by the next row
 }
@@ -546,6 +621,7 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
         S.need = 0;
         fence_mbar_init_cluster();
     }
+    for (int i = (int)threadIdx.x; i < NBC; i += (int)blockDim.x) S.hcnt[i] = 0u;
     __syncthreads();
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
