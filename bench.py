@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 
 from top_kl_distill_gb300 import workloads as W  # noqa: E402
 from top_kl_distill_gb300.slicing import cuts_for_slices  # noqa: E402
+from top_kl_distill_gb300.dist import max_over_ranks, world  # noqa: E402
 
 METRIC = "token-rows/sec and achieved HBM GB/s (% of GB300 peak) at 32000/128256 vocab"
 UNIT = "token-rows/s"
@@ -503,19 +504,11 @@ def oracle_rate(name, budget_s=8.0):
 
 
 def dist_setup():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return world()
 
 
 def barrier_max(torch, ws, value: float) -> float:
-    if ws == 1:
-        return value
-    import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t[0])
+    return max_over_ranks(value, "cuda") if ws > 1 else value
 
 
 def run_reference(args, ws, rank):
