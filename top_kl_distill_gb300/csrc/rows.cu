@@ -801,6 +801,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
     }
     if (c > 1) cluster_sync_all();
     else __syncthreads();
+    // launched as a programmatic dependent: the set-up above overlaps the tail of the
+    // previous kernel on the stream; its results are visible past this wait
+    pdl_wait_primary();
     pdl_launch_dependents();
 
     if (threadIdx.x < 32) {
@@ -856,14 +859,17 @@ cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters
     cfg.blockDim = dim3(NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = sizeof(Smem);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (P.csize > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)P.csize;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)P.csize;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     RowParams p = P;
     void* args[] = {&p};

@@ -623,6 +623,10 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
     }
     for (int i = (int)threadIdx.x; i < NBC; i += (int)blockDim.x) S.hcnt[i] = 0u;
     __syncthreads();
+    // launched as a programmatic dependent: the set-up above overlaps the tail of the
+    // previous kernel on the stream; its results are visible past this wait
+    pdl_wait_primary();
+    pdl_launch_dependents();
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
             producer(x, ld, V, ls, le, S);
@@ -663,8 +667,17 @@ cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long 
     const long long rows = le - ls;
     if (rows <= 0) return cudaSuccess;
     const unsigned grid = (unsigned)(rows < sms ? rows : sms);
-    topk_kernel<<<grid, NTHREADS, sizeof(TSmem), st>>>(x, ld, V, k, ls, le, ids, probs);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(TSmem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_kernel, x, ld, V, k, ls, le, ids, probs);
 }
 
 unsigned int topk_watchdog(bool clear) {

@@ -165,6 +165,7 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float h2, float l2)
 // kernel, griddepcontrol.wait holds it until the losses are in memory.
 __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ loss, long long ls, long long le,
                                                     float* __restrict__ mean) {
+    pdl_launch_dependents();                 // the next kernel may start its set-up
     pdl_wait_primary();
     __shared__ float2 red[32];
     float hi = 0.f, lo = 0.f;
