@@ -68,9 +68,9 @@ struct alignas(128) Smem {
     float ring[kSlots][kTileF];
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
-    uint64_t xbar[2];                   // cluster exchange of (max, sum)
+    uint64_t xbar[4];                   // cluster exchange of (max, sum)
     uint64_t lbar[2];                   // cluster exchange of KL loss parts (rank 0)
-    float2 xbuf[2][kMaxCluster];
+    float2 xbuf[4][kMaxCluster];
     float lbuf[2][kMaxCluster];
     float2 wred[2][NCW];
     float wloss[2][NCW];
@@ -533,6 +533,7 @@ struct Pending {
     bool has_ht;
     int jht;
     float ht;
+    uint32_t xb, xpar;   // cluster exchange buffer of its statistics and the phase to wait for
 };
 
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
@@ -597,6 +598,18 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     if (OP == kCeFused && rank == 0 && ct == LT) {
         if (!w.inwin) P.loss[w.r] = 0.f;
         else if (w.bad) P.loss[w.r] = __int_as_float(0x7fc00000);
+    }
+}
+
+// Cluster mode: the row's statistics from every rank's part (sent after its pass A).
+__device__ __forceinline__ void settle(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
+    wait_parity<true>(&S.xbar[w.xb], w.xpar, &S.abort, &g_watchdog);
+    const MaxSum tot = combine(S.xbuf[w.xb], P.csize);
+    w.m = tot.m;
+    w.lnS = logf(tot.s);
+    if (rank == 0 && ct == LT) {
+        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
+        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
     }
 }
 
@@ -721,24 +734,28 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         ++nred;
         if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
         named_sync(kBarConsumers, NCT);
-        MaxSum tot = combine(S.wred[b], NCW);
+        const MaxSum tot = combine(S.wred[b], NCW);
         if (c > 1) {
-            const uint32_t xb = nx & 1u, xpar = (nx >> 1) & 1u;
+            // send this CTA's part to every rank; the parts are collected just before this
+            // row's pass B, one row later, so the exchange overlaps the next pass A.  Four
+            // buffers: a peer writes buffer i + 4 only after its own collection of row
+            // i + 2, which needs this CTA's part of row i + 2, sent after row i was read.
+            cur.xb = nx & 3u;
+            cur.xpar = (nx >> 2) & 1u;
             ++nx;
             if (ct == 0) {
-                mbar_arrive_expect_tx(&S.xbar[xb], 8u * (uint32_t)c);
+                mbar_arrive_expect_tx(&S.xbar[cur.xb], 8u * (uint32_t)c);
                 for (int q = 0; q < c; ++q)
-                    st_async_f32x2(map_to_rank(&S.xbuf[xb][rank], (uint32_t)q), tot.m, tot.s,
-                                   map_to_rank(&S.xbar[xb], (uint32_t)q));
+                    st_async_f32x2(map_to_rank(&S.xbuf[cur.xb][rank], (uint32_t)q), tot.m, tot.s,
+                                   map_to_rank(&S.xbar[cur.xb], (uint32_t)q));
             }
-            wait_parity<true>(&S.xbar[xb], xpar, &S.abort, &g_watchdog);
-            tot = combine(S.xbuf[xb], c);
-        }
-        cur.m = tot.m;
-        cur.lnS = logf(tot.s);
-        if (rank == 0 && ct == LT) {
-            if (P.lse_out) P.lse_out[r] = cur.m + cur.lnS;
-            if (P.stats_out) { P.stats_out[2 * r] = cur.m; P.stats_out[2 * r + 1] = cur.lnS; }
+        } else {
+            cur.m = tot.m;
+            cur.lnS = logf(tot.s);
+            if (ct == LT) {
+                if (P.lse_out) P.lse_out[r] = cur.m + cur.lnS;
+                if (P.stats_out) { P.stats_out[2 * r] = cur.m; P.stats_out[2 * r + 1] = cur.lnS; }
+            }
         }
         if (kKL) {
             // this row's loss terms from the gathered logits
@@ -758,13 +775,19 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             if (rk2 >= 0) scatter_support(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
         }
         // ---- pass B of the previous row
-        if (pend.r >= 0) pass_b<OP>(P, S, pend, g, ct, lane, rank);
+        if (pend.r >= 0) {
+            if (c > 1) settle(P, S, pend, ct, rank);
+            pass_b<OP>(P, S, pend, g, ct, lane, rank);
+        }
         pend = cur;
         rk2 = rk1;
         rk1 = r;
         ++li;
     }
-    if (pend.r >= 0) pass_b<OP>(P, S, pend, g, ct, lane, rank);
+    if (pend.r >= 0) {
+        if (c > 1) settle(P, S, pend, ct, rank);
+        pass_b<OP>(P, S, pend, g, ct, lane, rank);
+    }
     if (kKL && li > 0) {
         named_sync(kBarConsumers, NCT);
         if (ct == 0) {
@@ -791,10 +814,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], NCW);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&S.xbar[b], 1u);      // the local expect_tx; the peers' data completes the bytes
-            mbar_init(&S.lbar[b], 1u);
-        }
+        for (int b = 0; b < 4; ++b) mbar_init(&S.xbar[b], 1u);   // the local expect_tx; the peers' data completes the bytes
+        for (int b = 0; b < 2; ++b) mbar_init(&S.lbar[b], 1u);
         S.abort = 0;
         S.issued = 0;
         fence_mbar_init_cluster();

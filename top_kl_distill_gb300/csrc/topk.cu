@@ -38,6 +38,8 @@ namespace {
 constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
+constexpr int kVecT = 2;                   // float4s of each tile per consumer thread
+constexpr int kTileT = 4 * NCT * kVecT;    // floats per tile (15 KB)
 constexpr int kSlotsT = 7;                 // ring tiles (105 KB)
 constexpr int RW = 512;                    // candidate entries per consumer warp
 constexpr int CB = RW * NCW;               // candidate buffer entries
@@ -48,11 +50,11 @@ constexpr int KOUT = KMAXT + SLACK;
 constexpr int DBC = 10;                    // digit bits of one exact cut round
 constexpr int NBC = 1024;                  // linear bins of a cut
 constexpr int NBK = 2048;                  // buckets of the final ordering
-constexpr int PER_TILE = kTileF / NCW;     // most candidates a warp can add per tile
+constexpr int PER_TILE = kTileT / NCW;     // most candidates a warp can add per tile
 constexpr int LIMIT_MAX = NCW * (RW - PER_TILE - 8);   // survivors that leave each region room for a tile
 constexpr uint32_t kBar = 1;
 
-static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
+static_assert(kTileT / 4 == NCT * kVecT, "kVecT float4s of each tile per consumer thread");
 static_assert(8 + PER_TILE <= RW, "the row's head and tail plus one tile fit an empty region");
 static_assert(KMAXT + KMAXT / 8 <= LIMIT_MAX, "cuts keep at most LIMIT_MAX");
 static_assert((1 << DBC) <= NBK && (NBK & (NBK - 1)) == 0, "histogram sizes");
@@ -61,7 +63,7 @@ static_assert(KOUT <= CB, "the final order is written over the candidate buffer"
 __device__ unsigned int g_watchdog;
 
 struct alignas(128) TSmem {
-    float ring[kSlotsT][kTileF];
+    float ring[kSlotsT][kTileT];
     uint64_t full[kSlotsT];
     uint64_t empty[kSlotsT];
     float cval[CB];                  // candidate values, region w = [w * RW, (w + 1) * RW)
@@ -113,13 +115,13 @@ __device__ void producer(const float* x, long long ld, long long V, long long ls
         int h = (4 - mis) & 3;
         if (h > V) h = (int)V;
         const int bt = ((int)V - h) & ~3;
-        for (int c0 = 0; c0 < bt; c0 += kTileF) {
+        for (int c0 = 0; c0 < bt; c0 += kTileT) {
             const uint32_t slot = g % kSlotsT, use = g / kSlotsT;
             if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog)) {
                 S.issued = g;
                 return;
             }
-            const uint32_t bytes = (uint32_t)min(kTileF, bt - c0) * 4u;
+            const uint32_t bytes = (uint32_t)min(kTileT, bt - c0) * 4u;
             mbar_arrive_expect_tx(&S.full[slot], bytes);
             bulk_g2s(S.ring[slot], rowp + h + c0, bytes, &S.full[slot]);
             ++g;
@@ -525,7 +527,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         if (h > V) h = (int)V;
         const int bt = ((int)V - h) & ~3;
         const int t0 = h + bt;
-        const int nt = (bt + kTileF - 1) / kTileF;
+        const int nt = (bt + kTileT - 1) / kTileT;
 
         uint32_t cnt = 0;          // this warp's candidates (same in every lane)
         float T = -INFINITY;       // admission threshold: everything until the first cut
@@ -568,10 +570,10 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
                     }
                 }
             }
-            const int n4 = min(kTileF, bt - t * kTileF) >> 2;
-            float4 v[kVec];
+            const int n4 = min(kTileT, bt - t * kTileT) >> 2;
+            float4 v[kVecT];
 #pragma unroll
-            for (int u = 0; u < kVec; ++u) {
+            for (int u = 0; u < kVecT; ++u) {
                 const int j = u * NCT + ct;
                 v[u] = j < n4 ? ld_shared_v4(&S.ring[slot][j * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
@@ -579,13 +581,13 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             if (lane == 0) mbar_arrive(&S.empty[slot]);
             const uint32_t before = cnt;
 #pragma unroll
-            for (int u = 0; u < kVec; ++u) {
+            for (int u = 0; u < kVecT; ++u) {
                 const int j = u * NCT + ct;
                 const bool active = j < n4;
                 // most float4s hold nothing at or above the threshold: one vote per warp
                 const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
                 if (__any_sync(0xffffffffu, any)) {
-                    const uint32_t c0 = (uint32_t)(h + t * kTileF + 4 * j);
+                    const uint32_t c0 = (uint32_t)(h + t * kTileT + 4 * j);
                     wappend(S, cw, cnt, any && v[u].x >= T, v[u].x, c0);
                     wappend(S, cw, cnt, any && v[u].y >= T, v[u].y, c0 + 1);
                     wappend(S, cw, cnt, any && v[u].z >= T, v[u].z, c0 + 2);

@@ -31,7 +31,7 @@ enum RowOp : int { kCeFused = 0, kCeFwd = 1, kCeBwd = 2, kKl = 3 };
 
 // Row-engine geometry limits (rows.cu).
 constexpr int kConsumerWarps = 15;        // + one producer warp: 16 warps, up to 128 registers a thread
-constexpr int kVec = 2;                   // float4s of each tile per consumer thread
+constexpr int kVec = 2;                   // row engine: float4s of each tile per consumer thread
 constexpr int kTileF = 4 * 32 * kConsumerWarps * kVec;   // floats per pipeline tile (15 KB)
 constexpr int kSlots = 12;                // tiles in the shared-memory ring (180 KB)
 constexpr int kMaxCluster = 8;
