@@ -58,6 +58,14 @@ constexpr int KSELF = 1024;             // teacher support per row, self-contain
 // behind the barrier of row i + 1, which every scatter of row i - 2 precedes.
 constexpr uint32_t kSupBufs = 4;
 constexpr uint32_t kBarConsumers = 1;   // named barrier id used by consumers only
+// Self-contained CE hands each warp's pass A partial to the row's pass B through
+// kPartBufs buffers and mbarriers, without a CTA barrier.  An mbarrier phase cannot
+// come round again before every warp, the waiter included, has arrived for it.  A
+// buffer's data is rewritten kPartBufs rows later; when every row has at least one
+// body tile per pass, a warp that far ahead of another would hold 2 kPartBufs - 2
+// tiles more than it, which the kSlots-tile ring does not allow.
+constexpr uint32_t kPartBufs = 8;
+static_assert(2 * kPartBufs - 2 > kSlots, "partial buffers outlast the ring");
 
 static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
 static_assert(KMAX >= 1024, "the C ABI promises k <= 1024");
@@ -73,6 +81,8 @@ struct alignas(128) Smem {
     float2 xbuf[4][kMaxCluster];
     float lbuf[2][kMaxCluster];
     float2 wred[2][NCW];
+    uint64_t abar[kPartBufs];           // self-contained CE: every warp's pass A partial is in
+    float2 wpart[kPartBufs][NCW];
     float wloss[2][NCW];
     union {
         struct {                        // streaming mode: support of the current row
@@ -534,6 +544,7 @@ struct Pending {
     int jht;
     float ht;
     uint32_t xb, xpar;   // cluster exchange buffer of its statistics and the phase to wait for
+    uint32_t ab, apar;   // CE: buffer of the warps' pass A partials and the phase to wait for
 };
 
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
@@ -601,6 +612,18 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     }
 }
 
+// Self-contained CE, one CTA per row: the row's statistics from the warps' partials.
+__device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w, int ct) {
+    wait_parity<false>(&S.abar[w.ab], w.apar, &S.abort, &g_watchdog);
+    const MaxSum tot = combine(S.wpart[w.ab], NCW);
+    w.m = tot.m;
+    w.lnS = logf(tot.s);
+    if (ct == LT) {
+        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
+        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
+    }
+}
+
 // Cluster mode: the row's statistics from every rank's part (sent after its pass A).
 __device__ __forceinline__ void settle(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
     wait_parity<true>(&S.xbar[w.xb], w.xpar, &S.abort, &g_watchdog);
@@ -632,6 +655,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const int c = P.csize;
     const int ncols = (int)P.ncols;
     const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
+    // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
+    const bool nobar = !kKL && c == 1 && ncols >= 8;
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
     long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (loss, support scatter owed)
     uint32_t nlab = 0, nid = 0;
@@ -730,6 +755,27 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         }
         g += (uint32_t)cur.nt;
         ms = ms_warp_reduce(ms);
+        if (nobar) {
+            // CE: publish this warp's partial and move on; the row's statistics are
+            // collected just before its pass B, one row later, when every warp has long
+            // arrived -- no CTA-wide barrier per row
+            cur.ab = nred % kPartBufs;
+            cur.apar = (nred / kPartBufs) & 1u;
+            ++nred;
+            if (lane == 0) {
+                S.wpart[cur.ab][cw] = make_float2(ms.m, ms.s);
+                mbar_arrive(&S.abar[cur.ab]);
+            }
+            if (pend.r >= 0) {
+                collect(P, S, pend, ct);
+                pass_b<OP>(P, S, pend, g, ct, lane, rank);
+            }
+            pend = cur;
+            rk2 = rk1;
+            rk1 = r;
+            ++li;
+            continue;
+        }
         const uint32_t b = nred & 1u;
         ++nred;
         if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
@@ -785,7 +831,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         ++li;
     }
     if (pend.r >= 0) {
-        if (c > 1) settle(P, S, pend, ct, rank);
+        if (nobar) collect(P, S, pend, ct);
+        else if (c > 1) settle(P, S, pend, ct, rank);
         pass_b<OP>(P, S, pend, g, ct, lane, rank);
     }
     if (kKL && li > 0) {
@@ -816,6 +863,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
         }
         for (int b = 0; b < 4; ++b) mbar_init(&S.xbar[b], 1u);   // the local expect_tx; the peers' data completes the bytes
         for (int b = 0; b < 2; ++b) mbar_init(&S.lbar[b], 1u);
+        for (int b = 0; b < kPartBufs; ++b) mbar_init(&S.abar[b], NCW);
         S.abort = 0;
         S.issued = 0;
         fence_mbar_init_cluster();
