@@ -74,6 +74,7 @@ struct alignas(128) TSmem {
     uint32_t oid[KOUT];
     uint32_t wtmp[2][NCW];
     uint32_t wcnt[NCW];
+    uint32_t wadm[NCW];              // values each warp admitted after a speculative cut
     float zred[NCW];
     uint32_t sel[4];
     uint32_t total;                  // candidates held, counted up as warps append
@@ -340,8 +341,8 @@ __device__ bool linear_cut(const uint32_t (&key)[NPER], uint32_t vmask, uint32_t
 
 // All consumer warps: cut the candidates of all regions (when there are more than K),
 // spread the survivors evenly over the regions and raise T.  cnt: this warp's count.
-__device__ __noinline__ void compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t& cnt,
-                                     float& T) {
+__device__ __noinline__ uint32_t compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t& cnt,
+                                         float& T) {
     const int cw = ct >> 5, lane = ct & 31;
     uint32_t key[NPER], id[NPER];
     const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
@@ -394,29 +395,96 @@ __device__ __noinline__ void compact(TSmem& S, uint32_t K, uint32_t limit, uint3
     cnt = (total + (uint32_t)(NCW - 1 - cw)) / (uint32_t)NCW;
     if (ct == 0) { S.total = total; S.need = 0; }
     named_sync(kBar, NCT);                 // regions rewritten, S.wcnt and S.wtmp read, flag lowered
+    return total;
 }
 
+// Per-row state of a consumer thread (the same in every thread of a warp; the cut
+// fields the same in every consumer thread).
+struct RowState {
+    uint32_t cnt;          // this warp's candidates
+    float T;               // admission threshold
+    uint32_t adm;          // values this warp admitted after the speculative cut
+    bool spec;             // the row runs with a speculative threshold
+    bool spec_pending;     // its first cut is still to come
+    uint32_t jspec;        // how many of the first tile's values that cut keeps
+    uint32_t spec_kept;    // how many it kept
+    bool valid_cut;        // a cut over the row's top K was made after it
+};
+
 // Entry of every warp into a collective step.  Returns how many warps had finished the
-// row; unless all had, the candidates are cut (compact) before returning.
-__device__ __forceinline__ uint32_t collective(TSmem& S, uint32_t K, uint32_t limit, int ct, uint32_t& cnt, float& T,
+// row; unless all had, the candidates are cut (compact) before returning.  The first
+// cut of a speculative row keeps about jspec candidates and sets a speculative T;
+// every later cut keeps the K largest (a lower bound of the row's K-th largest).
+__device__ __forceinline__ uint32_t collective(TSmem& S, RowState& st, uint32_t K, uint32_t limit, int ct,
                                                bool fin) {
     const int cw = ct >> 5, lane = ct & 31;
-    if (lane == 0) S.wcnt[cw] = cnt;
+    if (lane == 0) S.wcnt[cw] = st.cnt;
     const uint32_t nfin = named_sync_popc(kBar, NCT, fin && lane == 0);
     if (nfin == (uint32_t)NCW) return nfin;
     uint32_t tot = 0;
 #pragma unroll
     for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
     named_sync(kBar, NCT);                 // S.wcnt is rewritten by compact
-    compact(S, K, limit, tot, ct, cnt, T);
+    if (st.spec_pending) {
+        st.spec_pending = false;
+        st.adm = 0;                        // from here on admissions reach the speculative T
+        const uint32_t j = st.jspec;
+        st.spec_kept = compact(S, j, j + max(j / 8u, 16u), tot, ct, st.cnt, st.T);
+    } else {
+        compact(S, K, limit, tot, ct, st.cnt, st.T);
+        st.valid_cut |= tot > K;
+    }
     return nfin;
+}
+
+// Admission of one tile's values (absent ones -inf): those at or above T are appended
+// to this warp's region with one ballot per float4 group.  A warp that sees the
+// candidate total pass `trig` asks for a cut (not before a speculative row's first).
+__device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[kVecT], int n4, int h, int t,
+                                      int ct, uint32_t trig) {
+    const int cw = ct >> 5, lane = ct & 31;
+    const uint32_t before = st.cnt;
+    const float T = st.T;
+#pragma unroll
+    for (int u = 0; u < kVecT; ++u) {
+        const int j = u * NCT + ct;
+        const bool active = j < n4;
+        // most float4s hold nothing at or above the threshold: one vote per warp
+        const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
+        if (__any_sync(0xffffffffu, any)) {
+            const uint32_t c0 = (uint32_t)(h + t * kTileT + 4 * j);
+            wappend(S, cw, st.cnt, any && v[u].x >= T, v[u].x, c0);
+            wappend(S, cw, st.cnt, any && v[u].y >= T, v[u].y, c0 + 1);
+            wappend(S, cw, st.cnt, any && v[u].z >= T, v[u].z, c0 + 2);
+            wappend(S, cw, st.cnt, any && v[u].w >= T, v[u].w, c0 + 3);
+        }
+    }
+    const uint32_t added = st.cnt - before;
+    st.adm += added;
+    if (lane == 0 && added && !st.spec_pending) {
+        const uint32_t now = atomicAdd(&S.total, added) + added;
+        if (now > trig) S.need = 1;
+    }
 }
 
 // The end of a row, all warps: at most K + SLACK survivors, ordered by (value desc, id asc)
 // through 2048 buckets of the key range, the first K written with their probabilities.
-__device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t cnt, long long r, uint32_t* ids,
+// Returns false, doing nothing, when the row ran with a speculative threshold that
+// proved too high: fewer than K values at or above it and no exact cut since.
+__device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowState& st, long long r, uint32_t* ids,
                                         float* probs) {
     const int cw = ct >> 5, lane = ct & 31;
+    const uint32_t cnt = st.cnt;
+    if (st.spec && !st.valid_cut) {
+        uint32_t adm = st.spec_kept;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) adm += S.wadm[w];
+        if (adm < K) {
+            if (ct == 0) { S.total = 0; S.need = 0; }
+            named_sync(kBar, NCT);         // S.wcnt and S.wadm are read before the row is redone
+            return false;
+        }
+    }
     uint32_t tot = 0;
 #pragma unroll
     for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
@@ -507,6 +575,7 @@ __device__ __noinline__ void finish_row(TSmem& S, uint32_t K, int ct, uint32_t c
     for (int i = ct; i < NBC; i += NCT) S.hcnt[i] = 0u;
     if (ct == 0) { S.total = 0; S.need = 0; }
     named_sync(kBar, NCT);   // the regions, S.zred and S.total are reused by the next row
+    return true;
 }
 
 // ---------------------------------------------------------------- consumer
@@ -529,23 +598,44 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         const int t0 = h + bt;
         const int nt = (bt + kTileT - 1) / kTileT;
 
-        uint32_t cnt = 0;          // this warp's candidates (same in every lane)
-        float T = -INFINITY;       // admission threshold: everything until the first cut
-        // head and tail columns (at most 3 + 3) go to warp 0 unconditionally
-        if (cw == 0) {
-            bool keep = false;
-            float v = 0.f;
-            uint32_t id = 0;
-            if (ct < h) { id = (uint32_t)ct; v = rowp[id]; keep = true; }
-            else if (ct >= 4 && ct - 4 < (int)V - t0) { id = (uint32_t)(t0 + ct - 4); v = rowp[id]; keep = true; }
-            wappend(S, cw, cnt, keep, v, id);
+        // Speculation: the first tile's values are a sample of the row.  A threshold
+        // with about c j0 of them above it, j0 = K n / V the top-K members the sample
+        // holds on average, lets the rest of the row through at about c K values; the
+        // row's answer is exact when at least K of its values reach the threshold,
+        // which finish_row checks (the row is redone exactly when not).
+        RowState st;
+        st.cnt = 0;
+        st.T = -INFINITY;
+        st.adm = 0;
+        st.spec_kept = 0;
+        st.valid_cut = false;
+        {
+            const uint32_t n = (uint32_t)(min(kTileT, bt) + ((int)V - bt));
+            const float j0 = (float)K * (float)n / (float)V;
+            const uint32_t j = (uint32_t)ceilf((j0 >= 30.f ? 2.f : 3.f) * j0);
+            st.jspec = max(j, 1u);
+            st.spec = nt >= 8 && st.jspec <= n / 4u;
+            st.spec_pending = st.spec;
         }
+        // head and tail columns (at most 3 + 3) go to warp 0 unconditionally
+        auto head_tail = [&]() {
+            if (cw == 0) {
+                bool keep = false;
+                float v = 0.f;
+                uint32_t id = 0;
+                if (ct < h) { id = (uint32_t)ct; v = rowp[id]; keep = true; }
+                else if (ct >= 4 && ct - 4 < (int)V - t0) { id = (uint32_t)(t0 + ct - 4); v = rowp[id]; keep = true; }
+                wappend(S, cw, st.cnt, keep, v, id);
+            }
+        };
+        head_tail();
         for (int t = 0; t < nt; ++t) {
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlotsT, par = (gt / kSlotsT) & 1u;
-            // a cut first when another warp asks for one or this region has no room for a tile
-            if (__shfl_sync(0xffffffffu, *need, 0) || cnt + PER_TILE > (uint32_t)RW) {
+            // a cut first when another warp asks for one, this region has no room for a
+            // tile, or the speculative threshold is due (after the first tile)
+            if (__shfl_sync(0xffffffffu, *need, 0) || st.cnt + PER_TILE > (uint32_t)RW || (st.spec_pending && t == 1)) {
                 if (lane == 0) *need = 1;
-                collective(S, K, limit, ct, cnt, T, false);
+                collective(S, st, K, limit, ct, false);
             }
             // the tile; a cut asked for by another warp is joined while waiting
             {
@@ -554,7 +644,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
                 for (uint32_t it = 0;; ++it) {
                     if (__all_sync(0xffffffffu, mbar_try_wait(fb, par))) break;
                     if (__shfl_sync(0xffffffffu, *need, 0)) {
-                        collective(S, K, limit, ct, cnt, T, false);
+                        collective(S, st, K, limit, ct, false);
                         continue;
                     }
                     if ((it & 255u) == 255u) {
@@ -579,31 +669,41 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
-            const uint32_t before = cnt;
+            admit(S, st, v, n4, h, t, ct, trig);
+        }
+        g += (uint32_t)nt;
+        if (lane == 0) S.wadm[cw] = st.adm;
+        while (collective(S, st, K, limit, ct, true) != (uint32_t)NCW) {
+        }
+        if (finish_row(S, K, ct, st, r, ids, probs)) continue;
+
+        // ---- the speculative threshold was too high: the row again, exactly, read from
+        //      global memory (the ring has moved on to the next rows)
+        st.cnt = 0;
+        st.T = -INFINITY;
+        st.adm = 0;
+        st.spec = false;
+        st.spec_pending = false;
+        st.valid_cut = false;
+        head_tail();
+        for (int t = 0; t < nt; ++t) {
+            if (__shfl_sync(0xffffffffu, *need, 0) || st.cnt + PER_TILE > (uint32_t)RW) {
+                if (lane == 0) *need = 1;
+                collective(S, st, K, limit, ct, false);
+            }
+            const int n4 = min(kTileT, bt - t * kTileT) >> 2;
+            float4 v[kVecT];
 #pragma unroll
             for (int u = 0; u < kVecT; ++u) {
                 const int j = u * NCT + ct;
-                const bool active = j < n4;
-                // most float4s hold nothing at or above the threshold: one vote per warp
-                const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
-                if (__any_sync(0xffffffffu, any)) {
-                    const uint32_t c0 = (uint32_t)(h + t * kTileT + 4 * j);
-                    wappend(S, cw, cnt, any && v[u].x >= T, v[u].x, c0);
-                    wappend(S, cw, cnt, any && v[u].y >= T, v[u].y, c0 + 1);
-                    wappend(S, cw, cnt, any && v[u].z >= T, v[u].z, c0 + 2);
-                    wappend(S, cw, cnt, any && v[u].w >= T, v[u].w, c0 + 3);
-                }
+                v[u] = j < n4 ? *reinterpret_cast<const float4*>(rowp + h + t * kTileT + 4 * j)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
-            // many candidates overall: ask for a cut, which raises T
-            if (lane == 0 && cnt != before) {
-                const uint32_t now = atomicAdd(&S.total, cnt - before) + (cnt - before);
-                if (now > trig) *need = 1;
-            }
+            admit(S, st, v, n4, h, t, ct, trig);
         }
-        g += (uint32_t)nt;
-        while (collective(S, K, limit, ct, cnt, T, true) != (uint32_t)NCW) {
+        while (collective(S, st, K, limit, ct, true) != (uint32_t)NCW) {
         }
-        finish_row(S, K, ct, cnt, r, ids, probs);
+        finish_row(S, K, ct, st, r, ids, probs);
     }
 }
 
