@@ -74,7 +74,8 @@ struct alignas(128) TSmem {
     uint32_t oid[KOUT];
     uint32_t wtmp[2][NCW];
     uint32_t wcnt[NCW];
-    uint32_t wadm[NCW];              // values each warp admitted after a speculative cut
+    uint32_t wadm[NCW];              // values each warp admitted
+    float wspec[NCW];                // each warp's estimate of the speculative threshold
     float zred[NCW];
     uint32_t sel[4];
     uint32_t total;                  // candidates held, counted up as warps append
@@ -403,18 +404,16 @@ __device__ __noinline__ uint32_t compact(TSmem& S, uint32_t K, uint32_t limit, u
 struct RowState {
     uint32_t cnt;          // this warp's candidates
     float T;               // admission threshold
-    uint32_t adm;          // values this warp admitted after the speculative cut
+    uint32_t adm;          // values this warp admitted
     bool spec;             // the row runs with a speculative threshold
-    bool spec_pending;     // its first cut is still to come
-    uint32_t jspec;        // how many of the first tile's values that cut keeps
-    uint32_t spec_kept;    // how many it kept
-    bool valid_cut;        // a cut over the row's top K was made after it
+    bool spec_pending;     // which is set after the first tile
+    uint32_t aspec;        // rank, within a warp's share of the first tile, of its estimate
+    bool valid_cut;        // a cut over the row's K largest was made
 };
 
 // Entry of every warp into a collective step.  Returns how many warps had finished the
-// row; unless all had, the candidates are cut (compact) before returning.  The first
-// cut of a speculative row keeps about jspec candidates and sets a speculative T;
-// every later cut keeps the K largest (a lower bound of the row's K-th largest).
+// row; unless all had, the candidates are cut (compact) to the K largest, whose
+// smallest value becomes T (a lower bound of the row's K-th largest).
 __device__ __forceinline__ uint32_t collective(TSmem& S, RowState& st, uint32_t K, uint32_t limit, int ct,
                                                bool fin) {
     const int cw = ct >> 5, lane = ct & 31;
@@ -425,15 +424,8 @@ __device__ __forceinline__ uint32_t collective(TSmem& S, RowState& st, uint32_t 
 #pragma unroll
     for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
     named_sync(kBar, NCT);                 // S.wcnt is rewritten by compact
-    if (st.spec_pending) {
-        st.spec_pending = false;
-        st.adm = 0;                        // from here on admissions reach the speculative T
-        const uint32_t j = st.jspec;
-        st.spec_kept = compact(S, j, j + max(j / 8u, 16u), tot, ct, st.cnt, st.T);
-    } else {
-        compact(S, K, limit, tot, ct, st.cnt, st.T);
-        st.valid_cut |= tot > K;
-    }
+    compact(S, K, limit, tot, ct, st.cnt, st.T);
+    st.valid_cut |= tot > K;
     return nfin;
 }
 
@@ -467,6 +459,32 @@ __device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[
     }
 }
 
+// This warp's a-th largest of its values of the first tile (kVecT float4s a lane, all
+// present): a rounds of taking the warp's largest out.
+__device__ __forceinline__ float warp_kth(float4 (&v)[kVecT], uint32_t a, int lane) {
+    float e[4 * kVecT];
+#pragma unroll
+    for (int u = 0; u < kVecT; ++u) { e[4 * u] = v[u].x; e[4 * u + 1] = v[u].y; e[4 * u + 2] = v[u].z; e[4 * u + 3] = v[u].w; }
+    float top = -INFINITY;
+    for (uint32_t i = 0; i < a; ++i) {
+        float m = e[0];
+#pragma unroll
+        for (int q = 1; q < 4 * kVecT; ++q) m = fmaxf(m, e[q]);
+        top = m;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
+        // the lowest lane holding it takes one copy out
+        const uint32_t holders = __ballot_sync(0xffffffffu, m == top);
+        if (lane == __ffs(holders) - 1) {
+            bool done = false;
+#pragma unroll
+            for (int q = 0; q < 4 * kVecT; ++q)
+                if (!done && e[q] == top) { e[q] = -INFINITY; done = true; }
+        }
+    }
+    return top;
+}
+
 // The end of a row, all warps: at most K + SLACK survivors, ordered by (value desc, id asc)
 // through 2048 buckets of the key range, the first K written with their probabilities.
 // Returns false, doing nothing, when the row ran with a speculative threshold that
@@ -476,7 +494,7 @@ __device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowS
     const int cw = ct >> 5, lane = ct & 31;
     const uint32_t cnt = st.cnt;
     if (st.spec && !st.valid_cut) {
-        uint32_t adm = st.spec_kept;
+        uint32_t adm = 0;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) adm += S.wadm[w];
         if (adm < K) {
@@ -598,23 +616,23 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         const int t0 = h + bt;
         const int nt = (bt + kTileT - 1) / kTileT;
 
-        // Speculation: the first tile's values are a sample of the row.  A threshold
-        // with about c j0 of them above it, j0 = K n / V the top-K members the sample
-        // holds on average, lets the rest of the row through at about c K values; the
-        // row's answer is exact when at least K of its values reach the threshold,
-        // which finish_row checks (the row is redone exactly when not).
+        // Speculation: the first tile's values are a sample of the row, and a threshold
+        // estimated from it lets about 2.5 K values of the row through.  The row's answer
+        // is exact when at least K of its values reach the threshold (or a cut proved a
+        // higher bound), which finish_row checks; the row is redone exactly when not.
         RowState st;
         st.cnt = 0;
         st.T = -INFINITY;
         st.adm = 0;
-        st.spec_kept = 0;
         st.valid_cut = false;
         {
-            const uint32_t n = (uint32_t)(min(kTileT, bt) + ((int)V - bt));
-            const float j0 = (float)K * (float)n / (float)V;
-            const uint32_t j = (uint32_t)ceilf((j0 >= 30.f ? 2.f : 3.f) * j0);
-            st.jspec = max(j, 1u);
-            st.spec = nt >= 8 && st.jspec <= n / 4u;
+            // a warp's share of the first tile holds K * (kTileT / NCW) / V of the row's
+            // K largest on average; its estimate is the value with 2.5 times that many
+            // of its share at or above it, and the threshold is the mean of the warps'
+            // estimates, so that about 2.5 K values of the row pass it
+            const float share = (float)K * (float)(kTileT / NCW) / (float)V;
+            st.aspec = (uint32_t)ceilf(2.5f * share);
+            st.spec = nt >= 8 && st.aspec <= (uint32_t)(kTileT / NCW / 8);
             st.spec_pending = st.spec;
         }
         // head and tail columns (at most 3 + 3) go to warp 0 unconditionally
@@ -631,9 +649,8 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         head_tail();
         for (int t = 0; t < nt; ++t) {
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlotsT, par = (gt / kSlotsT) & 1u;
-            // a cut first when another warp asks for one, this region has no room for a
-            // tile, or the speculative threshold is due (after the first tile)
-            if (__shfl_sync(0xffffffffu, *need, 0) || st.cnt + PER_TILE > (uint32_t)RW || (st.spec_pending && t == 1)) {
+            // a cut first when another warp asks for one or this region has no room for a tile
+            if (__shfl_sync(0xffffffffu, *need, 0) || st.cnt + PER_TILE > (uint32_t)RW) {
                 if (lane == 0) *need = 1;
                 collective(S, st, K, limit, ct, false);
             }
@@ -669,6 +686,17 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
+            if (st.spec_pending) {
+                // first tile of a speculative row (every warp gets here before any cut)
+                const float e = warp_kth(v, st.aspec, lane);
+                if (lane == 0) S.wspec[cw] = e;
+                named_sync(kBar, NCT);
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) sum += S.wspec[w];
+                st.T = sum * (1.0f / NCW);
+                st.spec_pending = false;
+            }
             admit(S, st, v, n4, h, t, ct, trig);
         }
         g += (uint32_t)nt;
