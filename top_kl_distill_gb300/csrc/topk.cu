@@ -431,7 +431,8 @@ __device__ __forceinline__ uint32_t collective(TSmem& S, RowState& st, uint32_t 
 
 // Admission of one tile's values (absent ones -inf): those at or above T are appended
 // to this warp's region with one ballot per float4 group.  A warp that sees the
-// candidate total pass `trig` asks for a cut (not before a speculative row's first).
+// candidate total pass `trig` asks for a cut (not in a speculative row, where only a
+// full region does).
 __device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[kVecT], int n4, int h, int t,
                                       int ct, uint32_t trig) {
     const int cw = ct >> 5, lane = ct & 31;
@@ -453,7 +454,7 @@ __device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[
     }
     const uint32_t added = st.cnt - before;
     st.adm += added;
-    if (lane == 0 && added && !st.spec_pending) {
+    if (lane == 0 && added && !st.spec) {
         const uint32_t now = atomicAdd(&S.total, added) + added;
         if (now > trig) S.need = 1;
     }
@@ -627,11 +628,13 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         st.valid_cut = false;
         {
             // a warp's share of the first tile holds K * (kTileT / NCW) / V of the row's
-            // K largest on average; its estimate is the value with 2.5 times that many
-            // of its share at or above it, and the threshold is the mean of the warps'
-            // estimates, so that about 2.5 K values of the row pass it
+            // K largest on average; its estimate is the value with 1.7 times that many (at
+            // least 2) of its share at or above it, and the threshold is the mean of the
+            // warps' estimates: about 1.7 K values of the row pass it (the count check
+            // fails only when fewer than K do, far out in the tail for these ranks), and
+            // their regions keep room for a tile without a cut
             const float share = (float)K * (float)(kTileT / NCW) / (float)V;
-            st.aspec = (uint32_t)ceilf(2.5f * share);
+            st.aspec = max(2u, (uint32_t)ceilf(1.7f * share));
             st.spec = nt >= 8 && st.aspec <= (uint32_t)(kTileT / NCW / 8);
             st.spec_pending = st.spec;
         }
