@@ -9,24 +9,26 @@
 //
 //   * one persistent CTA per SM streams its rows through a ring of 15 KB tiles
 //     (1-D bulk copies, producer warp + 15 consumer warps, as the row engine);
-//   * each consumer warp owns a region of the shared candidate buffer.  A value
-//     enters its warp's region when it is at or above the running threshold T, a
-//     lower bound of the row's k-th largest value (the k-th largest of any subset
-//     of the row is one).  Warps stream independently: there is no barrier per tile;
-//   * a warp whose region could overflow on its next tile, or that sees the
-//     candidate total grow past a few times k, raises a shared flag; every warp
-//     checks it before each tile and while it waits for one, and all of them then
-//     cut the candidates together: a histogram of 10-bit digits of the
-//     order-preserving 32-bit keys (-0.0 folded into +0.0) over the key range
-//     present finds the bin holding the k-th largest key; everything from that
-//     bin's lower edge up is kept (at least k, at most k plus a small slack, a
-//     further digit round narrowing the bin when needed), spread evenly over the
-//     regions, and the lower edge becomes T.  Only when ties at one key exceed the
-//     slack is the cut made exact, the k-th key's ties kept by lowest column;
-//   * at the end of the row the survivors (at most k + 512) are placed into 2048
-//     buckets of the key range in descending order, ranked exactly by
-//     (value desc, id asc) within their bucket, and the first k written with
-//     their probabilities.
+//   * each consumer warp owns a region of the shared candidate buffer and streams
+//     its float4s of every tile on its own (no barrier per tile): values at or
+//     above the admission threshold T are appended with one ballot per float4 group;
+//   * speculation: on a long row each warp estimates, from its share of the first
+//     tile, the value that about 1.7 k of the row's values reach, and T starts at the
+//     warps' mean estimate.  The answer is exact when at least k values of the row
+//     reach T (or a cut below proved a higher bound), which the end of the row
+//     checks; otherwise the row is redone exactly, read again from global memory;
+//   * cuts: a warp whose region could overflow on its next tile (or, without
+//     speculation, that sees the candidate total pass a few times k) raises a
+//     shared flag; every warp checks it before each tile and while waiting for one,
+//     and all cut together: the candidates are counted into equal bins of their
+//     value range, everything from the bin holding the k-th largest up is kept
+//     (spread over the regions) and the smallest kept value becomes T, a lower bound
+//     of the row's k-th largest.  Crowded or degenerate ranges fall back to an exact
+//     MSD radix select over order-preserving keys (-0.0 folded into +0.0), the k-th
+//     key's ties kept by lowest column;
+//   * at the end of the row at most k + 1024 survivors are placed into 2048 value
+//     buckets in descending order, ranked exactly by (value desc, id asc) within
+//     their bucket, and the first k written with their probabilities.
 #include "vl_device.cuh"
 #include "vl_internal.h"
 
@@ -45,7 +47,7 @@ constexpr int RW = 512;                    // candidate entries per consumer war
 constexpr int CB = RW * NCW;               // candidate buffer entries
 constexpr int NPER = RW / 32;              // candidates per lane while cutting
 constexpr int KMAXT = 2048;
-constexpr int SLACK = 512;                 // survivors beyond k the final ordering takes
+constexpr int SLACK = 1024;                // survivors beyond k the final ordering takes
 constexpr int KOUT = KMAXT + SLACK;
 constexpr int DBC = 10;                    // digit bits of one exact cut round
 constexpr int NBC = 1024;                  // linear bins of a cut
