@@ -344,8 +344,17 @@ __device__ bool linear_cut(const uint32_t (&key)[NPER], uint32_t vmask, uint32_t
 
 // All consumer warps: cut the candidates of all regions (when there are more than K),
 // spread the survivors evenly over the regions and raise T.  cnt: this warp's count.
-__device__ __noinline__ uint32_t compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t& cnt,
-                                         float& T) {
+// What a cut leaves a warp: its candidate count, the threshold, and the total kept.
+struct CutOut {
+    uint32_t cnt;
+    float T;
+    uint32_t total;
+};
+
+// (Returned by value rather than through references, so that the callers' row state
+// stays in registers instead of local memory.)
+__device__ __noinline__ CutOut compact(TSmem& S, uint32_t K, uint32_t limit, uint32_t tot, int ct, uint32_t cnt,
+                                       float T) {
     const int cw = ct >> 5, lane = ct & 31;
     uint32_t key[NPER], id[NPER];
     const uint32_t vmask = load_region(S, cw, lane, cnt, key, id);
@@ -398,7 +407,7 @@ __device__ __noinline__ uint32_t compact(TSmem& S, uint32_t K, uint32_t limit, u
     cnt = (total + (uint32_t)(NCW - 1 - cw)) / (uint32_t)NCW;
     if (ct == 0) { S.total = total; S.need = 0; }
     named_sync(kBar, NCT);                 // regions rewritten, S.wcnt and S.wtmp read, flag lowered
-    return total;
+    return CutOut{cnt, T, total};
 }
 
 // Per-row state of a consumer thread (the same in every thread of a warp; the cut
@@ -426,7 +435,9 @@ __device__ __forceinline__ uint32_t collective(TSmem& S, RowState& st, uint32_t 
 #pragma unroll
     for (int w = 0; w < NCW; ++w) tot += S.wcnt[w];
     named_sync(kBar, NCT);                 // S.wcnt is rewritten by compact
-    compact(S, K, limit, tot, ct, st.cnt, st.T);
+    const CutOut o = compact(S, K, limit, tot, ct, st.cnt, st.T);
+    st.cnt = o.cnt;
+    st.T = o.T;
     st.valid_cut |= tot > K;
     return nfin;
 }
@@ -492,7 +503,7 @@ __device__ __forceinline__ float warp_kth(float4 (&v)[kVecT], uint32_t a, int la
 // through 2048 buckets of the key range, the first K written with their probabilities.
 // Returns false, doing nothing, when the row ran with a speculative threshold that
 // proved too high: fewer than K values at or above it and no exact cut since.
-__device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowState& st, long long r, uint32_t* ids,
+__device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowState st, long long r, uint32_t* ids,
                                         float* probs) {
     const int cw = ct >> 5, lane = ct & 31;
     const uint32_t cnt = st.cnt;
