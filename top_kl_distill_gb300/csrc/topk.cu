@@ -13,7 +13,7 @@
 //     its float4s of every tile on its own (no barrier per tile): values at or
 //     above the admission threshold T are appended with one ballot per float4 group;
 //   * speculation: on a long row each warp estimates, from its share of the first
-//     tile, the value that about 1.7 k of the row's values reach, and T starts at the
+//     tile, the value that about 1.4 k of the row's values reach, and T starts at the
 //     warps' mean estimate.  The answer is exact when at least k values of the row
 //     reach T (or a cut below proved a higher bound), which the end of the row
 //     checks; otherwise the row is redone exactly, read again from global memory;
@@ -641,13 +641,14 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         st.valid_cut = false;
         {
             // a warp's share of the first tile holds K * (kTileT / NCW) / V of the row's
-            // K largest on average; its estimate is the value with 1.7 times that many (at
+            // K largest on average; its estimate is the value with 1.4 times that many (at
             // least 2) of its share at or above it, and the threshold is the mean of the
-            // warps' estimates: about 1.7 K values of the row pass it (the count check
-            // fails only when fewer than K do, far out in the tail for these ranks), and
-            // their regions keep room for a tile without a cut
+            // warps' estimates: about 1.4 K values of the row pass it (the count check
+            // fails only when fewer than K do, about three standard deviations out for
+            // these ranks), their regions keep room for a tile without a cut, and the
+            // survivors fit the final ordering without one
             const float share = (float)K * (float)(kTileT / NCW) / (float)V;
-            st.aspec = max(2u, (uint32_t)ceilf(1.7f * share));
+            st.aspec = max(2u, (uint32_t)ceilf(1.4f * share));
             st.spec = nt >= 8 && st.aspec <= (uint32_t)(kTileT / NCW / 8);
             st.spec_pending = st.spec;
         }
