@@ -71,3 +71,11 @@ def test_topk_k_equals_v_and_misaligned():
 def test_topk_window_only():
     x = W.random_logits(10, 4000, seed=5)
     check(x, 64, ls=3, le=7)
+
+
+@pytest.mark.parametrize("k", [1, 256, 2048])
+def test_topk_tie_heavy_long_rows(k):
+    """Rows long enough for the speculative threshold, with many exact ties at it."""
+    x = W.tie_heavy_logits(6, 40000, seed=100 + k, step=0.25, sigma=1.5)
+    x[5] = np.float32(0.5)                     # one row all equal: every value ties
+    check(x, k)
