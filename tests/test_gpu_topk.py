@@ -79,3 +79,11 @@ def test_topk_tie_heavy_long_rows(k):
     x = W.tie_heavy_logits(6, 40000, seed=100 + k, step=0.25, sigma=1.5)
     x[5] = np.float32(0.5)                     # one row all equal: every value ties
     check(x, k)
+
+
+def test_topk_long_rows_misaligned_and_windowed():
+    """The speculative path with head and tail columns (odd row stride and offset) and a
+    loss window (rows outside it are left alone)."""
+    x = W.random_logits(9, 40007, seed=21, sigma=3.0)
+    check(x, 300, ls=1, le=8, ld=40011, off=3)
+    check(x, 2048, ls=2, le=9, ld=40011, off=1)
