@@ -270,11 +270,13 @@ def pin_kl_invariants(O):
     tp_m = np.array([[0.5, 0.25, 0.25]])
     sd = W.random_logits(1, 12, seed=34)
     _, gd = O.kl_topk(sd, tid_d, tp_d, 1.0)
-    _, gm = O.kl_topk(sd, tid_m, tp_m, 1.0)
+    lm, gm = O.kl_topk(sd, tid_m, tp_m, 1.0)
     _close(gd, gm, 1e-16, "repeated ids add their contributions")
-    # zero teacher probability: no loss term, no gradient change
-    _, gz = O.kl_topk(sd, np.array([[4, 9, 2, 7]]), np.array([[0.5, 0.25, 0.25, 0.0]]), 1.0)
-    _close(gz, gm, 1e-16, "p_T = 0 entries change nothing")
+    # zero teacher probability: no loss term (0 ln 0 = 0, the guard of kl_rows), no
+    # gradient change
+    lz, gz = O.kl_topk(sd, np.array([[4, 9, 2, 7]]), np.array([[0.5, 0.25, 0.25, 0.0]]), 1.0)
+    _close(gz, gm, 1e-16, "p_T = 0 entries change the gradient by nothing")
+    _close(lz, lm, 1e-16, "p_T = 0 entries add no loss term")
     # window: rows outside [loss_start, loss_end) have loss 0 and a zero gradient,
     # rows inside equal the unwindowed result
     lw, gw = O.kl_topk(s, tid, tp, coef, 2, 9)

@@ -35,6 +35,16 @@ MUTANTS = {
                                "order = (len(s) - 1 - np.argsort(-s[::-1], kind=\"stable\"))[:k]"),
     "topk probs over the row": ("probs[t] = e / e.sum()", "probs[t] = e / np.exp(s - v[0]).sum()"),
     "topk ascending": ("order = np.argsort(-s, kind=\"stable\")[:k]", "order = np.argsort(s, kind=\"stable\")[:k]"),
+    "ce forward ignores window": ("        if win[t]:\n            loss[t] = lse[t]", "        if True:\n            loss[t] = lse[t]"),
+    "ce backward ignores window": ("        if not win[t]:\n            continue\n        s = logits[t, col0",
+                                   "        s = logits[t, col0"),
+    "ce mean of empty window": ("    if n <= 0:\n        return 0.0\n", ""),
+    "ce slice part drops lse": ("part[t] = float(lse[t]) - s[j]", "part[t] = -s[j]"),
+    "topk ignores window": ("        if not win[t]:\n            continue\n        s = logits[t].astype(np.float64)\n        order",
+                            "        s = logits[t].astype(np.float64)\n        order"),
+    "kl keeps zero probabilities": ("            if pt > 0.0:\n                loss[t] +=", "            if True:\n                loss[t] +="),
+    "kl slice start excluded": ("if not (col0 <= j < col0 + ncols):", "if not (col0 < j < col0 + ncols):"),
+    "lse sum drops the max term": ("S = np.exp(s - m).sum()", "S = np.exp(s - m).sum() - 1.0"),
     "acc_add subtracts": ("return (a.astype(np.float64) + b.astype(np.float64)).astype(np.float32)",
                           "return (a.astype(np.float64) - b.astype(np.float64)).astype(np.float32)"),
     "acc_add truncates": ("return (a.astype(np.float64) + b.astype(np.float64)).astype(np.float32)",
