@@ -155,6 +155,9 @@ VL_API vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int
  * column (-0.0 equals +0.0); probs[t][q] = exp(s[ids[q]] - s[ids[0]]) / sum over the k.
  * The selection is exact (the page's per-thread best-8 is not).  Rows outside the window
  * are not written.  Logits must not hold NaN.  1 <= k <= min(V, VL_TOPK_KMAX).
+ * Time depends on the data: long rows are filtered with a threshold estimated from their
+ * first 3840 columns, and a row for which fewer than k values reach it (one sorted in
+ * descending order, for instance) is read a second time; the result is exact either way.
  *   ids [ntok][k] u32, probs [ntok][k] fp32.
  */
 VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
