@@ -68,3 +68,17 @@ def test_empty_calls_launch_nothing():
     vl.vl_ce_bwd_inplace(P, 10, 0, 10, 0, 10, None, None, None, 0, 0, 1.0, None, None, 0)
     vl.vl_kl_topk_inplace(P, 10, 0, 10, 0, 10, None, None, 3, 1.0, 0, 0, None, None, None, 0.0, None, None, 0)
     vl.vl_topk_rows(P, 10, 4, 10, 3, 2, 2, None, None, None, 0)
+
+
+def test_rejects_missing_outputs_and_huge_rows():
+    # KL without its teacher or loss pointer, top-k without its outputs
+    assert _status(vl.vl_kl_topk_inplace, P, 10, 4, 10, 0, 10, None, P, 3, 1.0, 0, 4,
+                   None, None, None, 0.0, P, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_kl_topk_inplace, P, 10, 4, 10, 0, 10, P, P, 3, 1.0, 0, 4,
+                   None, None, None, 0.0, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_topk_rows, P, 10, 4, 10, 3, 0, 4, None, P, None, 0) == vl.VL_EINVAL
+    # CE backward without labels; rows of 2^31 columns or more
+    assert _status(vl.vl_ce_bwd_inplace, P, 10, 4, 10, 0, 10, None, P, None, 0, 4, 1.0, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fwd, P, 1 << 31, 2, 1 << 31, P, 0, 2, P, None, None, None, None, 0) == vl.VL_EINVAL
+    # every failure leaves a message naming the entry point
+    assert "vl_ce_fwd" in vl.lib().vl_last_error_string().decode()
