@@ -247,13 +247,60 @@ class TopK(Case):
 
 
 class LargeV(Case):
-    """CE forward over full rows, then per vocabulary slice the in-place KL + CE gradient
-    from the row statistics, then acc_add of the slices' KL parts."""
+    """CE and top-k KL of 8192 rows x 128256 columns in one pass (vl_ce_kl_fused: each row
+    read once and its combined gradient written once, a row per 4-CTA cluster), and the
+    windowed CE mean."""
 
     def __init__(self, torch, w, nbuf):
         from top_kl_distill_gb300 import vloss as vl
         self.vl, self.w = vl, w
         self.name = w.name
+        self.launches_per_step = 2
+        self.pristine = _dev(torch, W.logits(w))
+        self.labels = _dev(torch, W.labels(w))
+        tid, tp = W.teacher(w)
+        self.tid, self.tp = _dev(torch, tid), _dev(torch, tp)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+        n = w.ntok
+        self.ce_loss = torch.zeros(n, device="cuda")
+        self.kl_loss = torch.zeros(n, device="cuda")
+        self.mean = torch.zeros(1, device="cuda")
+
+    def rows(self):
+        return self.w.ntok
+
+    def bytes_per_step(self):
+        w = self.w
+        # per row: read and write V fp32, the teacher's ids and probabilities, the label,
+        # both losses; plus the mean over the window
+        return w.ntok * (8 * w.V + 8 * w.k + 4 + 8) + (w.loss_end - w.loss_start) * 4 + 4
+
+    def kernel_bytes(self):
+        w = self.w
+        return w.ntok * (8 * w.V + 8 * w.k + 4 + 8)
+
+    def restore(self, j):
+        self.bufs[j].copy_(self.pristine)
+
+    def step(self, j, mean=True):
+        w = self.w
+        self.vl.vl_ce_kl_fused(self.bufs[j], w.V, w.ntok, w.V, self.labels, self.tid, self.tp, w.k, w.coef,
+                               w.ce_coef, w.loss_start, w.loss_end, self.kl_loss, self.ce_loss, None, None,
+                               self.mean if mean else None, None)
+
+    def kernel(self, j):
+        self.step(j, mean=False)
+
+
+class LargeVSliced(Case):
+    """The same step over two vocabulary slices of 64128 columns: CE forward over full
+    rows (row statistics), then per slice the in-place KL + CE gradient from them, then
+    acc_add of the slices' KL parts -- the slice API, 12 V bytes a row."""
+
+    def __init__(self, torch, w, nbuf):
+        from top_kl_distill_gb300 import vloss as vl
+        self.vl, self.w = vl, w
+        self.name = w.name + "_sliced"
         self.launches_per_step = 2 + w.slices
         self.pristine = _dev(torch, W.logits(w))
         self.labels = _dev(torch, W.labels(w))
@@ -266,6 +313,7 @@ class LargeV(Case):
         self.stats = torch.zeros((n, 2), device="cuda")
         self.mean = torch.zeros(1, device="cuda")
         self.parts = [torch.zeros(n, device="cuda") for _ in range(w.slices)]
+        self.kl_loss = self.parts[0]
         self.cuts = cuts_for_slices(w.V, w.slices)
 
     def rows(self):
@@ -309,7 +357,9 @@ def nbuf_for(bytes_per_buf: int) -> int:
 
 
 def base_workload(name):
-    return W.WORKLOADS[name.split("_k")[0] if name.startswith("topk") else name]
+    if name.startswith("topk"):
+        return W.WORKLOADS[name.split("_k")[0]]
+    return W.WORKLOADS[name[:-len("_sliced")] if name.endswith("_sliced") else name]
 
 
 def make_case(torch, name, ntok=None, nbuf=None):
@@ -325,7 +375,7 @@ def make_case(torch, name, ntok=None, nbuf=None):
         k = int(name.split("_k")[1]) if "_k" in name else w.k
         return TopK(torch, w, 1, k)
     if w.kind == "ce_kl_sliced":
-        return LargeV(torch, w, nb)
+        return LargeVSliced(torch, w, nb) if name.endswith("_sliced") else LargeV(torch, w, nb)
     raise ValueError(name)
 
 
@@ -399,26 +449,48 @@ def soak(torch, case, flush, until):
     return n
 
 
-def e2e_ce(torch, case, steps, warmup):
-    """The headline step through the C ABI from pinned host buffers: H2D of logits and labels,
-    vl_ce_fused, D2H of gradient, loss, lse and mean, all inside the timed region."""
-    w = case.w
+def e2e_ce(torch, case, steps, warmup, chunks=4, nstreams=2):
+    """The headline step end to end from pinned host buffers through the C ABI.
+
+    The batch goes in row chunks over `nstreams` streams, so that the upload of one
+    chunk, the fused call on another and the download of a third overlap: per chunk,
+    H2D of its logits and labels, vl_ce_fused over its rows (window clipped to them,
+    the batch's scale; a workspace per stream), D2H of its gradient, loss and lse.
+    Then vl_window_mean over the whole window and D2H of the mean.  All of it is inside
+    the timed region.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    w, vl = case.w, case.vl
+    n, V = w.ntok, w.V
     hx = torch.from_numpy(case.x_host).pin_memory()
     hl = torch.from_numpy(case.lab_host.view(np.int32)).pin_memory()
     hg = torch.empty_like(hx).pin_memory()
-    hloss = torch.empty(w.ntok).pin_memory()
-    hlse = torch.empty(w.ntok).pin_memory()
+    hloss = torch.empty(n).pin_memory()
+    hlse = torch.empty(n).pin_memory()
     hmean = torch.empty(1).pin_memory()
     x, lab = case.bufs[0], case.labels
+    streams = [torch.cuda.Stream() for _ in range(nstreams)]
+    wss = [torch.zeros(vl.VL_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda") for _ in range(nstreams)]
+    spans = [(i * n // chunks, (i + 1) * n // chunks) for i in range(chunks)]
+    main = torch.cuda.current_stream()
 
     def one():
-        x.copy_(hx, non_blocking=True)
-        lab.copy_(hl, non_blocking=True)
-        case.vl.vl_ce_fused(x, w.V, w.ntok, w.V, lab, w.loss_start, w.loss_end, w.scale, case.loss, case.lse,
-                            None, case.mean, None)
-        hg.copy_(x, non_blocking=True)
-        hloss.copy_(case.loss, non_blocking=True)
-        hlse.copy_(case.lse, non_blocking=True)
+        start = main.record_event()
+        for st in streams:
+            st.wait_event(start)
+        for i, (r0, r1) in enumerate(spans):
+            st = streams[i % nstreams]
+            with torch.cuda.stream(st):
+                x[r0:r1].copy_(hx[r0:r1], non_blocking=True)
+                lab[r0:r1].copy_(hl[r0:r1], non_blocking=True)
+                ls = min(max(w.loss_start - r0, 0), r1 - r0)
+                le = min(max(w.loss_end - r0, 0), r1 - r0)
+                vl.vl_ce_fused(x[r0:r1], V, r1 - r0, V, lab[r0:r1], ls, le, w.scale, case.loss[r0:r1],
+                               case.lse[r0:r1], None, None, None, wss[i % nstreams], st)
+                hg[r0:r1].copy_(x[r0:r1], non_blocking=True)
+                hloss[r0:r1].copy_(case.loss[r0:r1], non_blocking=True)
+                hlse[r0:r1].copy_(case.lse[r0:r1], non_blocking=True)
+        for st in streams:
+            main.wait_stream(st)
+        vl.vl_window_mean(case.loss, n, w.loss_start, w.loss_end, case.mean, main)
         hmean.copy_(case.mean, non_blocking=True)
 
     for _ in range(warmup):
@@ -431,11 +503,13 @@ def e2e_ce(torch, case, steps, warmup):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    # restore the pristine logits the other measurements use
+    # the host copies hold the step's results: check them against a device-only step
+    ref_g = x.clone()
     case.bufs[0].copy_(case.pristine)
     h2d = hx.numel() * 4 + hl.numel() * 4
-    d2h = hg.numel() * 4 + 2 * w.ntok * 4 + 4
-    return ms, h2d, d2h
+    d2h = hg.numel() * 4 + 2 * n * 4 + 4
+    ok = bool(torch.equal(hg.cuda(), ref_g))
+    return ms, h2d, d2h, ok
 
 
 def kernel_traffic(kernel_tag: str):
@@ -468,36 +542,141 @@ def roofline(case, kernel_ms, peak, peak_kind, tag):
             "algorithmic_bytes_per_launch": case.kernel_bytes()}
 
 
-KERNEL_TAG = {"ce_lm": "ce_fused", "ce_tiny": "ce_fused", "kl": "kl_resident", "large_v": "kl_sliced_stream"}
+KERNEL_TAG = {"ce_lm": "ce_fused", "ce_tiny": "ce_fused_tiny", "kl": "kl_resident", "large_v": "ce_kl_fused",
+              "large_v_sliced": "kl_sliced_stream"}
 
 
-def oracle_rate(name, budget_s=8.0):
-    """The CPU oracle, as it stands, on a bounded sample of the workload's rows.
-    Inputs are drawn outside the clock; only the oracle calls are timed."""
-    from oracle import vloss_oracle as O
-    w = W.WORKLOADS[name.split("_k")[0] if name.startswith("topk") else name]
+# ------------------------------------------------------------------ CPU oracle baseline
+#
+# The oracle, as it stands (float64 numpy, one row at a time), timed on the host's
+# cores: once in this process on one core, and on all cores with the rows split into
+# contiguous slices, one spawned worker process per slice (spawned, never forked: a
+# fork after the CUDA context exists can hang).  Inputs are drawn in the workers
+# before the clock starts; only the oracle calls are timed.
+
+def _oracle_inputs(name, r0, r1):
+    w = base_workload(name)
     k = int(name.split("_k")[1]) if "_k" in name else w.k
+    x = W.logits(w, r0, r1, threads=1)
+    lab = W.labels(w, r0, r1)
+    tid, tp = W.teacher(w, r0, r1) if w.k else (None, None)
+    return w, k, x, lab, tid, tp
+
+
+def _oracle_run(inp):
+    from oracle import vloss_oracle as O
+    w, k, x, lab, tid, tp = inp
+    n = x.shape[0]
+    if w.kind == "ce":
+        ls, le = 0, n
+        O.ce_fused(x, lab, ls, le, w.scale)
+    elif w.kind == "kl":
+        O.kl_topk(x, tid, tp, w.coef)
+    elif w.kind == "topk":
+        O.topk_rows(x, k)
+    else:
+        _, lse = O.ce_forward(x, lab, 0, n)
+        for c0, width in cuts_for_slices(w.V, w.slices):
+            O.kl_topk(x, tid, tp, w.coef, lse=lse, col0=c0, ncols=width, labels=lab, ce_coef=w.ce_coef)
+
+
+_WORKER_INPUTS = {}
+
+
+def _oracle_task(name, r0, r1, passes, barrier=None):
+    """In a worker: the oracle over rows [r0, r1), `passes` times; returns (rows, t0, t1)."""
+    key = (name, r0, r1)
+    if key not in _WORKER_INPUTS:
+        _WORKER_INPUTS.clear()
+        _WORKER_INPUTS[key] = _oracle_inputs(name, r0, r1)
+    inp = _WORKER_INPUTS[key]
+    if barrier is not None:
+        barrier.wait()
+    t0 = time.time()
+    for _ in range(passes):
+        _oracle_run(inp)
+    return (r1 - r0) * passes, t0, time.time()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_one_core(name, budget_s=2.0):
+    """Rows per second of the oracle on one core, over a bounded sample of the rows."""
+    w = base_workload(name)
     chunk, r, n, spent = 8, 0, 0, 0.0
     while spent < budget_s and n < w.ntok:
         r1 = min(w.ntok, r + chunk)
-        x = W.logits(w, r, r1, threads=1)
-        lab = W.labels(w, r, r1)
-        tid, tp = W.teacher(w, r, r1) if w.k else (None, None)
+        inp = _oracle_inputs(name, r, r1)
         t0 = time.perf_counter()
-        if w.kind == "ce":
-            O.ce_fused(x, lab, 0, r1 - r, w.scale)
-        elif w.kind == "kl":
-            O.kl_topk(x, tid, tp, w.coef)
-        elif w.kind == "topk":
-            O.topk_rows(x, k)
-        else:
-            _, lse = O.ce_forward(x, lab, 0, r1 - r)
-            for c0, width in cuts_for_slices(w.V, w.slices):
-                O.kl_topk(x, tid, tp, w.coef, lse=lse, col0=c0, ncols=width, labels=lab, ce_coef=w.ce_coef)
+        _oracle_run(inp)
         spent += time.perf_counter() - t0
         n += r1 - r
         r = r1
     return n / max(1e-9, spent), n, spent
+
+
+class OraclePool:
+    """One spawned worker per host core, each always given the same row slice, so that
+    its inputs are drawn once."""
+
+    def __init__(self, cores=None):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        self.cores = cores or host_cores()
+        ctx = mp.get_context("spawn")
+        self.ex = [cf.ProcessPoolExecutor(max_workers=1, mp_context=ctx) for _ in range(self.cores)]
+        self.mgr = ctx.Manager()
+
+    def slices(self, nrows):
+        n = min(nrows, self.cores)
+        return [(i * nrows // n, (i + 1) * nrows // n) for i in range(n)]
+
+    def timed(self, name, nrows, passes):
+        """All slices of rows [0, nrows), `passes` times each, started together; returns
+        (rows done, wall seconds from the common start to the last finish)."""
+        sl = self.slices(nrows)
+        bar = self.mgr.Barrier(len(sl))
+        futs = [self.ex[i].submit(_oracle_task, name, r0, r1, passes, bar) for i, (r0, r1) in enumerate(sl)]
+        res = [f.result() for f in futs]
+        rows = sum(r[0] for r in res)
+        return rows, max(r[2] for r in res) - min(r[1] for r in res)
+
+    def step(self, name, nrows):
+        """One pass over rows [0, nrows) split over the workers; wall seconds of the call."""
+        sl = self.slices(nrows)
+        t0 = time.perf_counter()
+        futs = [self.ex[i].submit(_oracle_task, name, r0, r1, 1) for i, (r0, r1) in enumerate(sl)]
+        for f in futs:
+            f.result()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for e in self.ex:
+            e.shutdown(wait=True)
+        self.mgr.shutdown()
+
+
+def oracle_baseline(name, pool, work_s=1.5):
+    """cpu_baseline: the oracle on all host cores (about work_s seconds of work a core)
+    plus the one-core figure it is sized from."""
+    w = base_workload(name)
+    r1, n1, s1 = oracle_one_core(name)
+    per_core = max(1, int(r1 * work_s))
+    want = per_core * pool.cores
+    nrows = min(w.ntok, want)
+    passes = max(1, round(want / nrows)) if nrows == w.ntok else 1
+    rows, wall = pool.timed(name, nrows, passes)
+    sample = (f"{passes} passes over all {w.ntok} rows" if nrows == w.ntok else f"rows 0-{nrows - 1} of {w.ntok}")
+    return {"value": round(rows / max(1e-9, wall), 2), "unit": UNIT, "cores": min(pool.cores, nrows), "kind": "oracle",
+            "sample": f"{sample}, float64 numpy, one spawned process per core, {wall:.1f} s wall "
+                      f"(input generation excluded)",
+            "one_core": {"value": round(r1, 2), "unit": UNIT, "cores": 1,
+                         "sample": f"{n1} rows, {s1:.1f} s on one core"}}
 
 
 # ------------------------------------------------------------------ main
@@ -512,34 +691,31 @@ def barrier_max(torch, ws, value: float) -> float:
 
 
 def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle, as it stands, on all host cores; one step is
+    one pass over the whole batch of the workload, its rows split over the cores."""
     if rank != 0:
         return
     name = args.workload
-    w = W.WORKLOADS[name]
-    from oracle import vloss_oracle as O
-    per_step_rows = 16
-    for _ in range(args.warmup):
-        x = W.logits(w, 0, per_step_rows, threads=1)
-        O.ce_fused(x, W.labels(w, 0, per_step_rows), 0, per_step_rows, w.scale)
-    total, rows = 0.0, 0
-    for s in range(args.steps):
-        r0 = (s * per_step_rows) % w.ntok
-        r1 = min(w.ntok, r0 + per_step_rows)
-        x = W.logits(w, r0, r1, threads=1)
-        lab = W.labels(w, r0, r1)
-        t0 = time.perf_counter()
-        O.ce_fused(x, lab, 0, r1 - r0, w.scale)
-        total += time.perf_counter() - t0
-        rows += r1 - r0
-    v = rows / total
+    w = base_workload(name)
+    pool = OraclePool()
+    try:
+        for _ in range(args.warmup):               # workers draw their inputs here
+            pool.step(name, w.ntok)
+        total = 0.0
+        for _ in range(args.steps):
+            total += pool.step(name, w.ntok)
+    finally:
+        pool.close()
+    v = w.ntok * args.steps / total
+    cores = min(pool.cores, w.ntok)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy)",
-        "config": {"workload": workload_desc(w), "step": f"{per_step_rows} rows of the batch per step"},
-        "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows ({per_step_rows} per step) of the {w.ntok}-row batch"},
+        "config": {"workload": workload_desc(w), "step": f"all {w.ntok} rows, split over {cores} host cores"},
+        "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} passes over the {w.ntok}-row batch, one spawned process per core"},
         "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -614,9 +790,9 @@ def main():
     rows_all = case.rows() * ws
     value = rows_all / (ms_step * 1e-3)
     kernel_ms = k_ms_total / args.steps
-    e2e_ms, h2d, d2h = (None, 0, 0)
+    e2e_ms, h2d, d2h, e2e_ok = (None, 0, 0, None)
     if isinstance(case, CeFused) and not args.no_oracle:
-        e2e_ms, h2d, d2h = e2e_ce(torch, case, max(10, args.steps // 4), 3)
+        e2e_ms, h2d, d2h, e2e_ok = e2e_ce(torch, case, max(10, args.steps // 4), 3)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -633,18 +809,19 @@ def main():
     }
     if e2e_ms is not None:
         line["e2e"] = {"value": round(case.rows() * ws / (e2e_ms * 1e-3), 1), "unit": UNIT,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
-    if rank == 0 and not args.no_oracle:
-        rate, nrows, secs = oracle_rate(args.workload)
-        line["cpu_baseline"] = {"value": round(rate, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{nrows} of {case.w.ntok} rows, {secs:.1f} s of float64 numpy "
-                                          f"on one host core (input generation excluded)"}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                       "pipeline": "4 row chunks over 2 streams: H2D, vl_ce_fused, D2H overlap; then "
+                                   "vl_window_mean and D2H of the mean",
+                       "host_gradient_matches_device": e2e_ok}
+    pool = OraclePool() if rank == 0 and not args.no_oracle else None
+    if pool is not None:
+        line["cpu_baseline"] = oracle_baseline(args.workload, pool)
     del case
     torch.cuda.empty_cache()
 
     if not args.no_sweep:
         sweep = {}
-        names = ["kl", "topk_k256", "topk_k2048", "large_v"]
+        names = ["ce_tiny", "kl", "topk_k256", "topk_k2048", "large_v", "large_v_sliced"]
         if args.sweep_only:
             names = [n for n in args.sweep_only.split(",") if n]
         for name in names:
@@ -660,14 +837,15 @@ def main():
                 "roofline": roofline(c, ktot / steps, peak, peak_kind, KERNEL_TAG.get(c.name, c.name)),
                 "gpu_launches": c.launches_per_step * steps,
             }
-            if rank == 0 and not args.no_oracle:
-                rate, nrows, secs = oracle_rate(name, budget_s=4.0)
-                entry["oracle_rows_per_s"] = round(rate, 2)
+            if pool is not None:
+                entry["cpu_baseline"] = oracle_baseline(name, pool, work_s=0.5)
             sweep[name] = entry
             del c
             torch.cuda.empty_cache()
         line["sweep"] = sweep
 
+    if pool is not None:
+        pool.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

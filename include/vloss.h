@@ -69,6 +69,8 @@ typedef enum vl_status {
 /* Limits of this build. */
 #define VL_KL_KMAX 1024      /* teacher support per row for vl_kl_topk_inplace */
 #define VL_TOPK_KMAX 2048    /* k of vl_topk_rows (the page's bound for topk_rows) */
+#define VL_MAX_COLS 0x7FFF0000LL   /* longest row V (2^31 - 2^16): rows are indexed with 32-bit ints */
+#define VL_WORKSPACE_BYTES 65536   /* size of the optional exchange workspace of vl_ce_fused */
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 VL_API int vl_version(void);
@@ -116,11 +118,20 @@ VL_API vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int6
  * Cross-entropy forward and backward in one pass over each row: the row is read from
  * HBM once and the gradient written once.  Outputs as vl_ce_fwd, then logits rows are
  * overwritten as vl_ce_bwd_inplace does with col0 = 0, ncols = V.
+ *   workspace (nullable): VL_WORKSPACE_BYTES bytes of device memory owned by the caller,
+ *     16-byte aligned and zero-filled before its first use.  With it, when the rows do
+ *     not divide evenly among the SMs, the rows left over after the last full wave are
+ *     cut into equal column ranges across all SMs (the parts exchange their row
+ *     statistics through the workspace), so no SM carries a whole extra row; results
+ *     are the same either way up to fp32 rounding.  Without it (NULL) a row stays on
+ *     one SM or one thread-block cluster.  Every call leaves the workspace ready for the
+ *     next one; calls that share a workspace must not overlap on the GPU (use one per
+ *     stream), or they race.
  */
 VL_API vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V,
                       const uint32_t* labels, int64_t loss_start, int64_t loss_end,
                       float scale, float* loss, float* lse, float* stats, float* mean,
-                      int32_t* err, void* stream);
+                      int32_t* err, void* workspace, void* stream);
 
 /*
  * Top-k distillation KL with the gradient written in place (train_head.rs: module doc,
@@ -150,19 +161,56 @@ VL_API vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int
                              float* loss, int32_t* err, void* stream);
 
 /*
+ * Cross-entropy and top-k distillation KL of the same rows in one pass (the loss step of
+ * train_head.rs head_kl -- one kl_rows over whole rows -- with the CE of
+ * wgpu_cross_entropy.rs): each row is read from HBM once and its combined gradient is
+ * written once, in place.  For rows t in the window:
+ *     logits[t][j] = (coef + ce_coef) * exp(s_j - lse_t) - coef * sum_{q: id_q = j} p_q
+ *                    - ce_coef * [j == label_t]
+ *     kl_loss[t]   = sum over q with p_q > 0 of p_q * (ln p_q - (s[id_q] - lse_t))
+ *     ce_loss[t]   = lse_t - s_t[label_t]  (NaN for a label >= V, counted in *err)
+ * Rows outside the window: both losses 0, gradient row zeroed, lse and stats not written.
+ * lse and stats (nullable) as vl_ce_fwd for the rows in the window; ce_mean (nullable) is
+ * the mean of ce_loss over the window (as read_loss).  Long rows are split over a
+ * thread-block cluster whose CTAs exchange their row statistics and loss parts through
+ * distributed shared memory.
+ *   labels [ntok] u32, tid [ntok][k] u32, tp [ntok][k] fp32 (as vl_kl_topk_inplace),
+ *   kl_loss [ntok] fp32, ce_loss [ntok] fp32.  1 <= k <= VL_KL_KMAX.
+ */
+VL_API vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V,
+                         const uint32_t* labels, const uint32_t* tid, const float* tp, int64_t k,
+                         float coef, float ce_coef, int64_t loss_start, int64_t loss_end,
+                         float* kl_loss, float* ce_loss, float* lse, float* stats, float* ce_mean,
+                         int32_t* err, void* stream);
+
+/*
  * Teacher top-k per row (train_head.rs: topk_rows): ids[t][q], q < k, are the columns of
  * the k largest logits of row t in descending order of value, ties broken by the lower
  * column (-0.0 equals +0.0); probs[t][q] = exp(s[ids[q]] - s[ids[0]]) / sum over the k.
  * The selection is exact (the page's per-thread best-8 is not).  Rows outside the window
- * are not written.  Logits must not hold NaN.  1 <= k <= min(V, VL_TOPK_KMAX).
+ * are not written.  1 <= k <= min(V, VL_TOPK_KMAX).  NaN is a data error: a NaN value is
+ * never selected, each row in the window that holds one adds 1 to *err (when err is not
+ * NULL), and a row with fewer than k other values gets id 0xFFFFFFFF and probability 0
+ * at the positions it cannot fill.  +-inf are ordinary values.
  * Time depends on the data: long rows are filtered with a threshold estimated from their
  * first 3840 columns, and a row for which fewer than k values reach it (one sorted in
  * descending order, for instance) is read a second time; the result is exact either way.
- *   ids [ntok][k] u32, probs [ntok][k] fp32.
+ *   ids [ntok][k] u32, probs [ntok][k] fp32, err: one int32 counter (nullable).
  */
 VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
                        int64_t loss_start, int64_t loss_end,
                        uint32_t* ids, float* probs, int32_t* err, void* stream);
+
+/*
+ * Windowed mean of per-row losses (wgpu_cross_entropy.rs: read_loss, which sums the
+ * losses and divides by loss_end - loss_start): *mean = sum of loss[loss_start, loss_end)
+ * / (loss_end - loss_start), 0 for an empty window.  The same reduction as the mean
+ * output of vl_ce_fwd / vl_ce_fused (a fixed-order double-float sum, so the result does
+ * not depend on the launch), for losses produced piecewise, e.g. by calls over chunks of
+ * the rows.  loss [ntok] fp32 (read only), mean: one fp32.
+ */
+VL_API vl_status vl_window_mean(const float* loss, int64_t ntok, int64_t loss_start, int64_t loss_end,
+                                float* mean, void* stream);
 
 /*
  * a[i] = a[i] + b[i] for 0 <= i < n, fp32, bit-exact (train_head.rs: acc_add, which adds a
@@ -170,6 +218,19 @@ VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int
  * a == b.
  */
 VL_API vl_status vl_acc_add(float* a, const float* b, int64_t n, void* stream);
+
+/*
+ * Test hook for the failure path (no counterpart on the pages).  Arms the next row-engine
+ * launch (vl_ce_fwd, vl_ce_bwd_inplace, vl_ce_fused, vl_kl_topk_inplace) made from the
+ * calling host thread: CTA 0 of that launch stops issuing its row tiles at body tile
+ * number withhold_tile (counted over the CTA's tiles in issue order), and every wait of
+ * the launch gives up after wait_cycles SM cycles instead of about two seconds.  The
+ * consumers' wait for the missing tile then runs out: the kernel raises the watchdog
+ * flag, lets the copies already issued land, and returns with that CTA's outputs
+ * incomplete; the other CTAs' rows are unaffected.  Nothing faults or hangs.
+ * 1000 <= wait_cycles <= 4e9.  The setting is used once, then cleared.
+ */
+VL_API vl_status vl_test_inject_wait_timeout(int64_t withhold_tile, int64_t wait_cycles);
 
 /*
  * Reads (and with clear != 0 resets) the flag that a kernel wait timed out on `device`.

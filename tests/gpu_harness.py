@@ -6,11 +6,10 @@ Tolerances (fp32 CUDA path against the float64 oracle):
   (scale for CE, coef + ce_coef for KL).  The kernels compute
   p = 2^(((s - m) - lnS) * log2 e); for large p the exponent is small and
   exact to a few ulp, so the relative error of p stays near 3e-7.
-* per-row losses: |dl| <= 1e-5 * |l| + floor, floor = 4 ulp(lse) + 64 * 2^-24.
-  A loss is lse - s[label] (or a p-weighted sum of such terms); lse carries a
-  rounding error of an ulp of itself plus the relative error of the fp32 sum S
-  (at most ~40 roundings of 2^-24), which bounds the absolute error whatever
-  the size of the loss.
+* per-row losses: |dl| <= 1e-5 * |l|, the stated bar.  Only rows whose loss is
+  far below their lse (|l| < 0.01 |lse|) get a floor of 4 ulp(lse) on top: a
+  loss is lse - s[label] (or a p-weighted sum of such terms), and lse carries a
+  rounding error of about an ulp of itself whatever the size of the loss.
 * lse: |d| <= 2 ulp(lse) + 64 * 2^-24 (same argument).
 * mean: |d| <= 1e-6 * |mean| + 1e-7.
 * top-k probabilities: |dp| <= 1e-5 * p + 1e-12; ids bit-exact.
@@ -74,18 +73,25 @@ def check_grad(got, want, c, what="gradient"):
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - want)
     tol = 1e-6 * abs(c)
-    bad = err > tol
-    assert not bad.any(), (f"{what}: {int(bad.sum())} elements off, max err {err.max():.3e} "
-                           f"(tol {tol:.3e}) at {np.unravel_index(np.argmax(err), err.shape)}")
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements off, max err {np.nanmax(err):.3e} "
+                           f"(tol {tol:.3e}) at {np.unravel_index(np.nanargmax(err), err.shape)}")
+    report(what, "max |dgrad|/c", float(err.max() / abs(c)) if err.size else 0.0)
 
 
 def check_loss(got, want, lse, what="loss"):
     got = np.asarray(got, dtype=np.float64)
-    floor = 4 * ulp(np.maximum(np.abs(lse), 1.0)) + 64 * EPS
+    want = np.asarray(want, dtype=np.float64)
+    lse = np.broadcast_to(np.asarray(lse, dtype=np.float64), want.shape)
+    small = np.abs(want) < 0.01 * np.abs(lse)
+    floor = np.where(small, 4 * ulp(np.maximum(np.abs(lse), 1.0)), 0.0)
     tol = 1e-5 * np.abs(want) + floor
     err = np.abs(got - want)
     bad = ~(err <= tol)
     assert not bad.any(), f"{what}: rows {np.nonzero(bad)[0][:10]} off, max err {np.nanmax(err):.3e}"
+    big = ~small & (want != 0)
+    report(what, "max |dloss|/|loss|", float(np.max(err[big] / np.abs(want[big]))) if big.any() else 0.0)
+    report(what, "rows under the lse floor", int(small.sum()))
 
 
 def check_lse(got, want, what="lse"):
@@ -106,3 +112,19 @@ def check_probs(got, want, what="probs"):
     tol = 1e-5 * np.abs(want) + 1e-12
     bad = ~(err <= tol)
     assert not bad.any(), f"{what}: {int(bad.sum())} off, max err {np.nanmax(err):.3e}"
+    pos = want > 0
+    report(what, "max |dp|/p", float(np.max(err[pos] / want[pos])) if pos.any() else 0.0)
+
+
+def report(what, quantity, value):
+    """Append an observed error to the file named by VL_PARITY_LOG (when set), one JSON
+    line per check, so that a GPU run can record how far inside its tolerance each
+    workload lands."""
+    import json
+    import os
+    path = os.environ.get("VL_PARITY_LOG")
+    if not path:
+        return
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": test, "check": what, "quantity": quantity, "value": value}) + "\n")

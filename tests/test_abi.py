@@ -27,10 +27,10 @@ P = 1 << 20
 
 
 def test_rejects_bad_rows():
-    assert _status(vl.vl_ce_fused, P, 10, 4, 11, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
-    assert _status(vl.vl_ce_fused, P, 10, 4, 0, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
-    assert _status(vl.vl_ce_fused, P, 10, -1, 10, P, 0, 0, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
-    assert _status(vl.vl_ce_fused, None, 10, 4, 10, P, 0, 4, 1.0, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, P, 10, 4, 11, P, 0, 4, 1.0, P, None, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, P, 10, 4, 0, P, 0, 4, 1.0, P, None, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, P, 10, -1, 10, P, 0, 0, 1.0, P, None, None, None, None, None, 0) == vl.VL_EINVAL
+    assert _status(vl.vl_ce_fused, None, 10, 4, 10, P, 0, 4, 1.0, P, None, None, None, None, None, 0) == vl.VL_EINVAL
 
 
 def test_rejects_bad_windows():
@@ -82,3 +82,38 @@ def test_rejects_missing_outputs_and_huge_rows():
     assert _status(vl.vl_ce_fwd, P, 1 << 31, 2, 1 << 31, P, 0, 2, P, None, None, None, None, 0) == vl.VL_EINVAL
     # every failure leaves a message naming the entry point
     assert "vl_ce_fwd" in vl.lib().vl_last_error_string().decode()
+
+
+def test_row_length_limit():
+    """Rows are indexed with 32-bit ints: the longest accepted row is VL_MAX_COLS
+    (2^31 - 2^16) columns, checked on the host before anything is launched."""
+    big = vl.VL_MAX_COLS
+    assert _status(vl.vl_ce_fwd, P, big + 1, 2, big + 1, P, 0, 2, P, None, None, None, None, 0) == vl.VL_EINVAL
+    assert str(big) in vl.lib().vl_last_error_string().decode()
+    for fn, args in [
+        (vl.vl_ce_fused, (P, big + 1, 3, big + 1, P, 0, 3, 1.0, P, None, None, None, None, None, 0)),
+        (vl.vl_ce_bwd_inplace, (P, big + 1, 3, big + 1, 0, 8, P, P, None, 0, 3, 1.0, None, None, 0)),
+        (vl.vl_kl_topk_inplace, (P, big + 1, 3, big + 1, 0, big + 1, P, P, 3, 1.0, 0, 3,
+                                 None, None, None, 0.0, P, None, 0)),
+        (vl.vl_topk_rows, (P, big + 1, 3, big + 1, 3, 0, 3, P, P, None, 0)),
+    ]:
+        assert _status(fn, *args) == vl.VL_EINVAL, fn.__name__
+    # exactly VL_MAX_COLS passes the checks (no rows: nothing is launched)
+    vl.vl_ce_fwd(P, big, 0, big, None, 0, 0, None, None, None, None, None, 0)
+
+
+def test_workspace_alignment_checked():
+    assert _status(vl.vl_ce_fused, P, 10, 4, 10, P, 0, 4, 1.0, P, None, None, None, None, P + 4, 0) == vl.VL_EINVAL
+    assert "aligned" in vl.lib().vl_last_error_string().decode()
+
+
+def test_wait_timeout_hook_rejects_bad_settings():
+    for args in [(-1, 10_000), (0, 10), (0, 5_000_000_000)]:
+        assert _status(vl.vl_test_inject_wait_timeout, *args) == vl.VL_EINVAL
+
+
+def test_window_mean_host_checks():
+    assert _status(vl.vl_window_mean, P, 10, 3, 2, P, 0) == vl.VL_EINVAL       # window reversed
+    assert _status(vl.vl_window_mean, P, 10, 0, 11, P, 0) == vl.VL_EINVAL      # past ntok
+    assert _status(vl.vl_window_mean, P, 10, 0, 4, None, 0) == vl.VL_EINVAL    # no output
+    assert _status(vl.vl_window_mean, None, 10, 0, 4, P, 0) == vl.VL_EINVAL    # no losses

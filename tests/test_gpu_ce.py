@@ -16,7 +16,7 @@ def _vl():
     return vloss
 
 
-def run_fused(x, lab, ls, le, scale, ld=None, off=0):
+def run_fused(x, lab, ls, le, scale, ld=None, off=0, workspace="auto"):
     torch = H.torch_cuda()
     vl = _vl()
     ntok, V = x.shape
@@ -29,7 +29,7 @@ def run_fused(x, lab, ls, le, scale, ld=None, off=0):
     mean = torch.full((1,), -7.0, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     vl.vl_ce_fused(view.data_ptr() if ntok else buf.data_ptr(), ld, ntok, V, labels, ls, le, scale, loss, lse,
-                   stats, mean, err)
+                   stats, mean, err, workspace)
     torch.cuda.synchronize()
     return buf, view, loss, lse, stats, mean, err
 
@@ -48,8 +48,9 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("ws", ["split", "whole_rows"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_ce_fused(name):
+def test_ce_fused(name, ws):
     if name == "tiny_workload":
         w = W.WORKLOADS["ce_tiny"]
         x, lab = W.logits(w), W.labels(w)
@@ -59,7 +60,8 @@ def test_ce_fused(name):
         x = W.random_logits(ntok, V, seed=zlib.crc32(name.encode()), sigma=sigma)
         lab = W.random_labels(ntok, V, seed=zlib.crc32(name.encode()) + 1)
     ntok, V = x.shape
-    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
+    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off,
+                                                       "auto" if ws == "split" else None)
     oloss, olse, og, omean = O.ce_fused(x, lab, ls, le, scale)
     g = H.host(view)
     H.check_grad(g[:, :V], og, scale)
@@ -171,3 +173,53 @@ def test_ce_fused_beyond_on_chip_rows():
     H.check_grad(H.host(view), og, scale)
     H.check_loss(H.host(loss), oloss, olse)
     H.check_mean(H.host(mean)[0], omean)
+
+
+@pytest.mark.parametrize("ntok,V,ld,off", [
+    (1, 4000, 4000, 0),          # one row over every SM
+    (151, 3000, 3001, 1),        # one row short of a wave: ragged stride, misaligned base
+    (152, 3000, 3000, 0),        # exactly one wave per SM count of a GB300 (no tail)
+    (153, 2999, 3003, 3),        # one row past a wave
+    (300, 1003, 1003, 2),
+    (457, 7, 9, 1),              # rows shorter than a float4 run
+    (512, 32000, 32000, 0),      # the LM workload's shape
+])
+def test_ce_fused_tail_split(ntok, V, ld, off):
+    """The rows past the last full wave cut across all SMs: every row, its lse, loss and
+    gradient, whatever the cut points, alignment and stride; two calls in a row on the
+    same workspace (its generation advances) both match."""
+    seed = ntok * 7919 + V
+    x = W.random_logits(ntok, V, seed=seed, sigma=3.0)
+    lab = W.random_labels(ntok, V, seed=seed + 1)
+    ls, le, scale = ntok // 5, ntok, 1.0 / max(1, ntok - ntok // 5)
+    oloss, olse, og, omean = O.ce_fused(x, lab, ls, le, scale)
+    for _ in range(2):
+        buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
+        g = H.host(view)
+        H.check_grad(g[:, :V], og, scale, "split gradient")
+        if ld > V:
+            assert np.isnan(g[:, V:]).all()
+        if off:
+            assert np.isnan(H.host(buf)[:off]).all()
+        H.check_loss(H.host(loss), oloss, olse, "split loss")
+        H.check_lse(H.host(lse), olse, "split lse")
+        st = H.host(stats)
+        assert np.array_equal(st[:, 0], x.max(axis=1))
+        H.check_mean(H.host(mean)[0], omean)
+        assert int(H.host(err)[0]) == 0
+
+
+def test_ce_fused_split_bad_labels_counted_once():
+    """A bad label in a row cut over several SMs is counted once and gives a NaN loss."""
+    ntok, V = 40, 20000
+    x = W.random_logits(ntok, V, seed=71)
+    lab = W.random_labels(ntok, V, seed=72)
+    lab[[0, 17, 39]] = [V, V + 5, 0xFFFFFFFF]
+    _, view, loss, _, _, _, err = run_fused(x, lab, 0, ntok, 0.5)
+    assert int(H.host(err)[0]) == 3
+    l = H.host(loss)
+    assert np.isnan(l[[0, 17, 39]]).all()
+    ok = np.setdiff1d(np.arange(ntok), [0, 17, 39])
+    oloss, olse, og, _ = O.ce_fused(x, np.where(lab < V, lab, 0).astype(np.uint32), 0, ntok, 0.5)
+    H.check_loss(l[ok], oloss[ok], olse[ok])
+    H.check_grad(H.host(view)[ok], og[ok], 0.5)

@@ -9,7 +9,7 @@ from top_kl_distill_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def run_topk(x, k, ls=0, le=None, ld=None, off=0):
+def run_topk(x, k, ls=0, le=None, ld=None, off=0, with_err=False):
     torch = H.torch_cuda()
     from top_kl_distill_gb300 import vloss as vl
     ntok, V = x.shape
@@ -18,15 +18,18 @@ def run_topk(x, k, ls=0, le=None, ld=None, off=0):
     _, view = H.strided(x, ld, off)
     ids = torch.full((ntok, k), -1, dtype=torch.int32, device="cuda")
     probs = torch.full((ntok, k), -1.0, device="cuda")
-    vl.vl_topk_rows(view.data_ptr(), ld, ntok, V, k, ls, le, ids, probs)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vl.vl_topk_rows(view.data_ptr(), ld, ntok, V, k, ls, le, ids, probs, err)
     torch.cuda.synchronize()
-    return H.host(ids).view(np.uint32), H.host(probs)
+    out = H.host(ids).view(np.uint32), H.host(probs)
+    return out + (int(H.host(err)[0]),) if with_err else out
 
 
 def check(x, k, ls=0, le=None, **kw):
     ntok = x.shape[0]
     le = ntok if le is None else le
-    ids, probs = run_topk(x, k, ls, le, **kw)
+    ids, probs, err = run_topk(x, k, ls, le, with_err=True, **kw)
+    assert err == 0
     oids, oprobs, valid = O.topk_rows(x, k, ls, le)
     assert np.array_equal(ids[valid].astype(np.int64), oids[valid]), "top-k ids differ"
     H.check_probs(probs[valid], oprobs[valid])
@@ -87,3 +90,48 @@ def test_topk_long_rows_misaligned_and_windowed():
     x = W.random_logits(9, 40007, seed=21, sigma=3.0)
     check(x, 300, ls=1, le=8, ld=40011, off=3)
     check(x, 2048, ls=2, le=9, ld=40011, off=1)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+def test_topk_tiny_rows(V):
+    """Rows shorter than one float4 run: only head and tail columns (no bulk copy), at
+    every base misalignment and with k = V, k = 1 and a middle k."""
+    x = W.tie_heavy_logits(7, V, seed=300 + V, step=0.5, sigma=1.0)
+    for off in range(4):
+        for k in sorted({1, max(1, V // 2), V}):
+            check(x, k, ld=V + (off & 1), off=off)
+
+
+def test_topk_nan_rows_counted():
+    """NaN is a data error: never selected, one count per row in the window that holds
+    one.  Rows with at least k other values get the top k of those values."""
+    x = W.random_logits(7, 5000, seed=41, sigma=2.0)
+    x[1, [7, 100, 4999]] = np.nan
+    x[4, 0] = np.nan                          # a head column (offset 1 below)
+    x[6, 2] = np.nan                          # outside the window: not counted
+    ids, probs, err = run_topk(x, 64, 0, 6, off=1, with_err=True)
+    assert err == 2
+    xo = np.where(np.isnan(x), -np.inf, x).astype(np.float32)
+    oids, oprobs, valid = O.topk_rows(xo, 64, 0, 6)
+    assert np.array_equal(ids[valid].astype(np.int64), oids[valid])
+    H.check_probs(probs[valid], oprobs[valid])
+    # a long row (speculative threshold) with a NaN in its body
+    y = W.random_logits(3, 40000, seed=42, sigma=3.0)
+    y[2, 12345] = np.nan
+    ids, probs, err = run_topk(y, 256, with_err=True)
+    assert err == 1
+    oids, oprobs, _ = O.topk_rows(np.where(np.isnan(y), -np.inf, y).astype(np.float32), 256)
+    assert np.array_equal(ids.astype(np.int64), oids)
+
+
+def test_topk_row_with_fewer_values_than_k():
+    x = W.random_logits(2, 50, seed=43)
+    x[1, 5:] = np.nan                          # five values left in row 1
+    ids, probs, err = run_topk(x, 10, with_err=True)
+    assert err == 1
+    oids, oprobs, _ = O.topk_rows(x[:1], 10)
+    assert np.array_equal(ids[0].astype(np.int64), oids[0])
+    o5, p5, _ = O.topk_rows(x[1:, :5], 5)
+    assert np.array_equal(ids[1, :5].astype(np.int64), o5[0])
+    H.check_probs(probs[1, :5], p5[0])
+    assert np.all(ids[1, 5:] == 0xFFFFFFFF) and np.all(probs[1, 5:] == 0.0)

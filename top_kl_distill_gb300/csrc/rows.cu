@@ -78,9 +78,9 @@ struct alignas(128) Smem {
     uint64_t empty[kSlots];
     uint64_t xbar[4];                   // cluster exchange of (max, sum)
     uint64_t lbar[2];                   // cluster exchange of KL loss parts (rank 0)
-    float2 xbuf[4][kMaxCluster];
+    float4 xbuf[4][kMaxCluster];        // (max, sum, KL a, KL b) of each rank's part
     float lbuf[2][kMaxCluster];
-    float2 wred[2][NCW];
+    float4 wred[2][NCW];                // per warp: (max, sum, KL a, KL b)
     uint64_t abar[kPartBufs];           // self-contained CE: every warp's pass A partial is in
     float2 wpart[kPartBufs][NCW];
     float wloss[2][NCW];
@@ -93,7 +93,6 @@ struct alignas(128) Smem {
         struct {                        // self-contained mode: support of the last kSupBufs rows
             int ecol[kSupBufs][KSELF];       // support column (slice-relative; -1 elsewhere)
             float ep[kSupBufs][KSELF];
-            float wl2[2][NCW];               // KL loss per warp, summed one row later
         };
     };
     int abort;
@@ -132,6 +131,109 @@ __device__ __forceinline__ Part part_of(const float* rowp, int n, int rank, int 
     p.lo = rank == 0 ? 0 : h + s;
     p.hi = rank == c - 1 ? n : h + e;
     return p;
+}
+
+// Columns of units [u0, u1) of a row slice of n floats, cut into U = ceil(n / 4) units:
+// unit u is body float4 min(u, nb4) (nb4 body float4s after the head); the head goes
+// with the part that starts at unit 0, the tail with the part that ends at unit U.
+// The parts of any partition of [0, U) cover the row exactly once.
+__device__ __forceinline__ Part part_units(const float* rowp, int n, int U, int u0, int u1) {
+    Part p;
+    const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
+    int h = (4 - mis) & 3;
+    if (h > n) h = n;
+    const int nb4 = (n - h) >> 2;
+    const int f0 = min(u0, nb4), f1 = min(u1, nb4);
+    p.h = h;
+    p.hn = u0 == 0 ? h : 0;
+    p.b0 = h + 4 * f0;
+    p.bn = 4 * (f1 - f0);
+    p.t0 = h + 4 * nb4;
+    p.tn = u1 == U ? n - p.t0 : 0;
+    p.lo = u0 == 0 ? 0 : p.b0;
+    p.hi = u1 == U ? n : p.b0 + p.bn;
+    return p;
+}
+
+// ---------------------------------------------------------------- tail split
+//
+// With G CTAs and R rows, every CTA first takes q = R / G whole rows (b, b + G, ...).
+// The T = R - qG rows left over are not given whole to T of the CTAs (which would leave
+// the others idle for a row's time): their units, T * U in all, are cut into G equal
+// ranges, CTA b taking units [b TU / G, (b + 1) TU / G).  A range is shorter than a
+// row, so it touches at most two rows: the CTA's tail segments 0 and 1.  A segment's
+// (max, sum) is published in the workspace; before a segment's pass B its CTA merges
+// the parts of the row from every CTA that holds one, in CTA order, so that all of
+// them use bit-identical row statistics.
+//
+// Workspace words: [0] generation, [1] ticket, then slot (b, s) at word
+// 4 + 4 (2b + s) = {max, sum, sequence, -}.  A launch reads the generation g at its
+// start and marks its slots with sequence g + 1; the last CTA to finish (ticket)
+// advances the generation, so a launch never reads a slot left by an earlier one.
+
+struct Item {
+    long long r;     // row
+    int u0, u1;      // units [u0, u1) of the row
+    int which;       // -1: a whole row; 0 / 1: this CTA's first / second tail segment
+    long long j;     // tail row index (which >= 0)
+};
+
+__device__ __forceinline__ bool item_at(const RowParams& P, long long i, int U, Item& it) {
+    const long long G = gridDim.x, b = blockIdx.x;
+    const long long q = P.ntok / G;
+    if (i < q) {
+        it.r = b + i * G;
+        it.u0 = 0;
+        it.u1 = U;
+        it.which = -1;
+        it.j = -1;
+        return true;
+    }
+    const long long TU = (P.ntok - q * G) * (long long)U;
+    const long long lo = b * TU / G, hi = (b + 1) * TU / G;
+    if (lo >= hi) return false;
+    const long long j0 = lo / U, j1 = (hi - 1) / U;
+    if (i == q) {
+        it.j = j0;
+        it.u0 = (int)(lo - j0 * U);
+        it.u1 = (int)(min(hi, (j0 + 1) * U) - j0 * U);
+    } else if (i == q + 1 && j1 > j0) {
+        it.j = j1;
+        it.u0 = 0;
+        it.u1 = (int)(hi - j1 * U);
+    } else {
+        return false;
+    }
+    it.which = (int)(i - q);
+    it.r = q * G + it.j;
+    return true;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned int* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int* ws_slot(const RowParams& P, long long b, int which) {
+    return P.ws + kWsHeaderWords + 4 * (2 * b + which);
+}
+
+// This CTA's (max, sum) of tail segment `which`, for the other parts of its row.
+__device__ __forceinline__ void publish_part(const RowParams& P, int which, MaxSum ms, uint32_t epoch) {
+    unsigned int* sl = ws_slot(P, blockIdx.x, which);
+    asm volatile("st.global.cg.v2.f32 [%0], {%1, %2};" :: "l"(sl), "f"(ms.m), "f"(ms.s) : "memory");
+    st_release_u32(sl + 2, epoch);
 }
 
 template <int OP>
@@ -173,23 +275,48 @@ __device__ __forceinline__ void ms_addv(MaxSum& a, const float4 (&v)[kVec]) {
     a.s += t;
 }
 
-__device__ __forceinline__ float max4(const float4& v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
-
 // ---------------------------------------------------------------- producer
 
 // Issue the body tiles of one row part; false if a wait gave up.
-__device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long long r, int rank, uint32_t& g) {
-    const float* rowp = P.x + r * P.ld + P.col0;
-    const Part pt = part_of(rowp, (int)P.ncols, rank, P.csize);
+__device__ __forceinline__ bool issue_body(const RowParams& P, Smem& S, const float* rowp, const Part& pt,
+                                           uint32_t& g) {
     for (int c0 = 0; c0 < pt.bn; c0 += kTileF) {
+        // test hook: CTA 0 stops before this tile, so the consumers' wait for it runs out
+        if ((long long)g == P.withhold && blockIdx.x == 0) return false;
         const uint32_t slot = g % kSlots, use = g / kSlots;
-        if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog)) return false;
+        if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog, P.wait_limit)) return false;
         const uint32_t bytes = (uint32_t)min(kTileF, pt.bn - c0) * 4u;
         mbar_arrive_expect_tx(&S.full[slot], bytes);
         bulk_g2s(S.ring[slot], rowp + pt.b0 + c0, bytes, &S.full[slot]);
         ++g;
     }
     return true;
+}
+
+__device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long long r, int rank, uint32_t& g) {
+    const float* rowp = P.x + r * P.ld + P.col0;
+    return issue_body(P, S, rowp, part_of(rowp, (int)P.ncols, rank, P.csize), g);
+}
+
+__device__ __forceinline__ bool issue_item(const RowParams& P, Smem& S, const Item& it, int U, uint32_t& g) {
+    const float* rowp = P.x + it.r * P.ld + P.col0;
+    return issue_body(P, S, rowp, part_units(rowp, (int)P.ncols, U, it.u0, it.u1), g);
+}
+
+// Tail split: the items (whole rows, then tail segments) in the two-pass order.
+__device__ void producer_split(const RowParams& P, Smem& S) {
+    const int U = (int)((P.ncols + 3) >> 2);
+    uint32_t g = 0;
+    Item it, prev;
+    bool have_prev = false, ok = true;
+    for (long long i = 0; ok && item_at(P, i, U, it); ++i) {
+        ok = issue_item(P, S, it, U, g);
+        if (ok && have_prev) ok = issue_item(P, S, prev, U, g);
+        prev = it;
+        have_prev = true;
+    }
+    if (ok && have_prev && !S.abort) issue_item(P, S, prev, U, g);
+    S.issued = g;
 }
 
 // Tile order: one pass per row for the streaming and reduce modes; for the
@@ -212,10 +339,10 @@ __device__ void producer(const RowParams& P, Smem& S, int rank, long long cid, l
 }
 
 // Before the CTA exits, every bulk copy it issued must have landed.
-__device__ void drain(Smem& S) {
+__device__ void drain(Smem& S, long long limit) {
     const uint32_t iss = S.issued;
     for (uint32_t gt = iss > (uint32_t)kSlots ? iss - kSlots : 0u; gt < iss; ++gt)
-        wait_parity_drain(&S.full[gt % kSlots], (gt / kSlots) & 1u);
+        wait_parity_drain(&S.full[gt % kSlots], (gt / kSlots) & 1u, limit);
 }
 
 // ---------------------------------------------------------------- consumer helpers
@@ -264,6 +391,27 @@ __device__ __forceinline__ MaxSum combine(const float2* part, int n) {
     return MaxSum{M, T};
 }
 
+// Row partials with the KL loss parts: (max, sum) combined as above, and the sums
+// a = sum p (ln p - s), b = sum p over the teacher support entries the parts hold.
+// KL = sum p (ln p - (s - lse)) = a + lse * b, so the loss needs no statistics until
+// the parts meet.
+struct Part4 {
+    MaxSum ms;
+    float a, b;
+};
+
+__device__ __forceinline__ Part4 combine4(const float4* part, int n) {
+    float M = part[0].x;
+    for (int i = 1; i < n; ++i) M = fmaxf(M, part[i].x);
+    float T = 0.f, A = 0.f, B = 0.f;
+    for (int i = 0; i < n; ++i) {
+        T += part[i].y * ex2((part[i].x - M) * kLog2e);
+        A += part[i].z;
+        B += part[i].w;
+    }
+    return Part4{MaxSum{M, T}, A, B};
+}
+
 // ---------------------------------------------------------------- consumer
 
 template <int OP, bool RES>
@@ -273,7 +421,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
     const int cw = ct >> 5, lane = ct & 31;
     const int c = P.csize;
     const int ncols = (int)P.ncols;
-    uint32_t g = 0, nred = 0, nloss = 0, nx = 0, nlx = 0, nrow = 0;
+    uint32_t g = 0, nred = 0, nloss = 0, nlx = 0, nrow = 0;
     const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
     const float cg = P.cg;
     // the label and support entry q = ct of the next row, loaded one row ahead
@@ -351,7 +499,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
             if (has_ht) ms_add(ms, ht);
             for (int t = 0; t < nt; ++t) {
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
-                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
                 const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
 #pragma unroll
                 for (int u = 0; u < kVec; ++u) {
@@ -367,21 +515,9 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
             ms = ms_warp_reduce(ms);
             const uint32_t b = nred & 1u;
             ++nred;
-            if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
+            if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, 0.f, 0.f);
             named_sync(kBarConsumers, NCT);
-            MaxSum tot = combine(S.wred[b], NCW);
-            if (RES && c > 1) {
-                const uint32_t xb = nx & 1u, xpar = (nx >> 1) & 1u;
-                ++nx;
-                if (ct == 0) {
-                    mbar_arrive_expect_tx(&S.xbar[xb], 8u * (uint32_t)c);
-                    for (int q = 0; q < c; ++q)
-                        st_async_f32x2(map_to_rank(&S.xbuf[xb][rank], (uint32_t)q), tot.m, tot.s,
-                                       map_to_rank(&S.xbar[xb], (uint32_t)q));
-                }
-                wait_parity<true>(&S.xbar[xb], xpar, &S.abort, &g_watchdog);
-                tot = combine(S.xbuf[xb], c);
-            }
+            const MaxSum tot = combine4(S.wred[b], NCW).ms;
             m = tot.m;
             lnS = logf(tot.s);
             if (rank == 0 && ct == LT) {
@@ -410,7 +546,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
             const uint64_t pol = l2_evict_first();
             for (int t = 0; t < nt; ++t) {
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
-                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+                wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
                 const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
 #pragma unroll
                 for (int u = 0; u < kVec; ++u) {
@@ -518,7 +654,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                     if (rank == 0) mbar_arrive_expect_tx(&S.lbar[lb], 4u * (uint32_t)c);
                     st_async_f32(map_to_rank(&S.lbuf[lb][rank], 0u), L, map_to_rank(&S.lbar[lb], 0u));
                     if (rank == 0) {
-                        wait_parity<true>(&S.lbar[lb], lpar, &S.abort, &g_watchdog);
+                        wait_parity<true>(&S.lbar[lb], lpar, &S.abort, &g_watchdog, P.wait_limit);
                         float T = 0.f;
                         for (int q = 0; q < c; ++q) T += S.lbuf[lb][q];
                         P.loss[r] = T;
@@ -545,13 +681,17 @@ struct Pending {
     float ht;
     uint32_t xb, xpar;   // cluster exchange buffer of its statistics and the phase to wait for
     uint32_t ab, apar;   // CE: buffer of the warps' pass A partials and the phase to wait for
+    bool first;          // this part holds column 0 of the row: it writes lse, stats, out-of-window loss
+    int which;           // tail split: -1 whole row, else the tail segment
+    long long j;         // tail split: tail row index
 };
 
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
 // label's one-hot folded in.  The teacher support is left to scatter_support.
 template <int OP>
-__device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
-                                       int rank) {
+__device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane) {
+    // the CE loss: the fused CE output, or beside the KL when labels come with it
+    float* const ce_out = OP == kCeFused ? P.loss : OP == kKl ? P.ce_loss : nullptr;
     const float c1 = w.inwin ? P.cg : 0.f;
     // c1 * exp(d - lnS) = 2^(d * log2e - K) with K = lnS * log2e - log2(c1), for c1 >= 0
     const bool fold = c1 >= 0.f;
@@ -561,7 +701,7 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     const float K = fold ? w.lnS * kLog2e - log2f(c1) : 0.f;
     for (int t = 0; t < w.nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
-        wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+        wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
         const int n4 = min(kTileF, w.pt.bn - t * kTileF) >> 2;
         float4 v[kVec];
 #pragma unroll
@@ -590,7 +730,7 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
                     if (d < 4u) {
                         const float xs = d == 0 ? x.x : d == 1 ? x.y : d == 2 ? x.z : x.w;
                         sub_at(o, d, P.ce_coef);
-                        if (OP == kCeFused) P.loss[w.r] = (w.m - xs) + w.lnS;
+                        if (ce_out) ce_out[w.r] = (w.m - xs) + w.lnS;
                     }
                 }
                 st_global_v4_hint(w.rowp + c0, o, pol);
@@ -602,19 +742,19 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
         float o = c1 * soft(w.ht, w.m, w.lnS);
         if (w.inwin && w.jht == w.jl) {
             o -= P.ce_coef;
-            if (OP == kCeFused) P.loss[w.r] = (w.m - w.ht) + w.lnS;
+            if (ce_out) ce_out[w.r] = (w.m - w.ht) + w.lnS;
         }
         w.rowp[w.jht] = o;
     }
-    if (OP == kCeFused && rank == 0 && ct == LT) {
-        if (!w.inwin) P.loss[w.r] = 0.f;
-        else if (w.bad) P.loss[w.r] = __int_as_float(0x7fc00000);
+    if (ce_out && w.first && ct == LT) {
+        if (!w.inwin) ce_out[w.r] = 0.f;
+        else if (w.bad) ce_out[w.r] = __int_as_float(0x7fc00000);
     }
 }
 
 // Self-contained CE, one CTA per row: the row's statistics from the warps' partials.
 __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w, int ct) {
-    wait_parity<false>(&S.abar[w.ab], w.apar, &S.abort, &g_watchdog);
+    wait_parity<false>(&S.abar[w.ab], w.apar, &S.abort, &g_watchdog, P.wait_limit);
     const MaxSum tot = combine(S.wpart[w.ab], NCW);
     w.m = tot.m;
     w.lnS = logf(tot.s);
@@ -624,15 +764,18 @@ __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w,
     }
 }
 
-// Cluster mode: the row's statistics from every rank's part (sent after its pass A).
+// Cluster mode: the row's statistics (and KL loss parts) from every rank's part, sent
+// after its pass A.  Every rank combines the parts in rank order: the same bits.
+template <int OP>
 __device__ __forceinline__ void settle(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
-    wait_parity<true>(&S.xbar[w.xb], w.xpar, &S.abort, &g_watchdog);
-    const MaxSum tot = combine(S.xbuf[w.xb], P.csize);
-    w.m = tot.m;
-    w.lnS = logf(tot.s);
+    wait_parity<true>(&S.xbar[w.xb], w.xpar, &S.abort, &g_watchdog, P.wait_limit);
+    const Part4 tot = combine4(S.xbuf[w.xb], P.csize);
+    w.m = tot.ms.m;
+    w.lnS = logf(tot.ms.s);
     if (rank == 0 && ct == LT) {
         if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
         if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
+        if (OP == kKl) P.loss[w.r] = fmaf(w.m + w.lnS, tot.b, tot.a);
     }
 }
 
@@ -654,7 +797,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const int cw = ct >> 5, lane = ct & 31;
     const int c = P.csize;
     const int ncols = (int)P.ncols;
-    const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
+    const bool has_label = (OP != kKl) || P.labels != nullptr;
     // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
     const bool nobar = !kKL && c == 1 && ncols >= 8;
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
@@ -679,7 +822,10 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         const bool inwin = r >= P.ls && r < P.le;
         if (!row_loaded<OP>(P, r)) {
             zero_part(rowp, pt, ct);
-            if (ct == 0 && rank == 0) P.loss[r] = 0.f;
+            if (ct == 0 && rank == 0) {
+                P.loss[r] = 0.f;
+                if (P.ce_loss) P.ce_loss[r] = 0.f;
+            }
             continue;
         }
         const uint32_t sb = li % kSupBufs;
@@ -689,6 +835,9 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         cur.pt = pt;
         cur.nt = (pt.bn + kTileF - 1) / kTileF;
         cur.inwin = inwin;
+        cur.first = rank == 0;
+        cur.which = -1;
+        cur.j = -1;
         cur.jl = -1;
         cur.bad = false;
         if (has_label) {
@@ -732,6 +881,17 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                 }
             }
         }
+        // KL loss parts of the support entries this thread holds: a = sum p (ln p - s),
+        // b = sum p (the loss is a + lse * b; entries with p <= 0 add no term)
+        float ka = 0.f, kb = 0.f;
+        if (kKL) {
+#pragma unroll
+            for (int i = 0; i < EPT; ++i)
+                if (scol[i] >= 0 && sp[i] > 0.f) {
+                    ka += sp[i] * (logf(sp[i]) - sx[i]);
+                    kb += sp[i];
+                }
+        }
         cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
         cur.jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
         cur.ht = cur.has_ht ? rowp[cur.jht] : 0.f;
@@ -741,7 +901,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         if (cur.has_ht) ms_add(ms, cur.ht);
         for (int t = 0; t < cur.nt; ++t) {
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
-            wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog);
+            wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
             const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
             float4 v[kVec];
 #pragma unroll
@@ -768,7 +928,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             }
             if (pend.r >= 0) {
                 collect(P, S, pend, ct);
-                pass_b<OP>(P, S, pend, g, ct, lane, rank);
+                pass_b<OP>(P, S, pend, g, ct, lane);
             }
             pend = cur;
             rk2 = rk1;
@@ -778,9 +938,13 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         }
         const uint32_t b = nred & 1u;
         ++nred;
-        if (lane == 0) S.wred[b][cw] = make_float2(ms.m, ms.s);
+        if (kKL) {
+            ka = warp_sum(ka);
+            kb = warp_sum(kb);
+        }
+        if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, ka, kb);
         named_sync(kBarConsumers, NCT);
-        const MaxSum tot = combine(S.wred[b], NCW);
+        const Part4 tot = combine4(S.wred[b], NCW);
         if (c > 1) {
             // send this CTA's part to every rank; the parts are collected just before this
             // row's pass B, one row later, so the exchange overlaps the next pass A.  Four
@@ -790,40 +954,27 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             cur.xpar = (nx >> 2) & 1u;
             ++nx;
             if (ct == 0) {
-                mbar_arrive_expect_tx(&S.xbar[cur.xb], 8u * (uint32_t)c);
+                mbar_arrive_expect_tx(&S.xbar[cur.xb], 16u * (uint32_t)c);
+                const float4 mine = make_float4(tot.ms.m, tot.ms.s, tot.a, tot.b);
                 for (int q = 0; q < c; ++q)
-                    st_async_f32x2(map_to_rank(&S.xbuf[cur.xb][rank], (uint32_t)q), tot.m, tot.s,
+                    st_async_f32x4(map_to_rank(&S.xbuf[cur.xb][rank], (uint32_t)q), mine,
                                    map_to_rank(&S.xbar[cur.xb], (uint32_t)q));
             }
         } else {
-            cur.m = tot.m;
-            cur.lnS = logf(tot.s);
+            cur.m = tot.ms.m;
+            cur.lnS = logf(tot.ms.s);
             if (ct == LT) {
                 if (P.lse_out) P.lse_out[r] = cur.m + cur.lnS;
                 if (P.stats_out) { P.stats_out[2 * r] = cur.m; P.stats_out[2 * r + 1] = cur.lnS; }
+                if (kKL) P.loss[r] = fmaf(cur.m + cur.lnS, tot.b, tot.a);
             }
         }
-        if (kKL) {
-            // this row's loss terms from the gathered logits
-            float lacc = 0.f;
-#pragma unroll
-            for (int i = 0; i < EPT; ++i)
-                if (scol[i] >= 0 && sp[i] > 0.f) lacc += sp[i] * (logf(sp[i]) - ((sx[i] - cur.m) - cur.lnS));
-            lacc = warp_sum(lacc);
-            if (lane == 0) S.wl2[li & 1u][cw] = lacc;
-            // past this row's barrier: the previous row's loss terms are all in, and
-            // pass B of the row two back is done
-            if (ct == 0 && rk1 >= 0) {
-                float L = 0.f;
-                for (int w = 0; w < NCW; ++w) L += S.wl2[(li + 1u) & 1u][w];
-                P.loss[rk1] = L;
-            }
-            if (rk2 >= 0) scatter_support(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
-        }
+        // past this row's barrier, pass B of the row two back is done: its support terms
+        if (kKL && rk2 >= 0) scatter_support(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
         // ---- pass B of the previous row
         if (pend.r >= 0) {
-            if (c > 1) settle(P, S, pend, ct, rank);
-            pass_b<OP>(P, S, pend, g, ct, lane, rank);
+            if (c > 1) settle<OP>(P, S, pend, ct, rank);
+            pass_b<OP>(P, S, pend, g, ct, lane);
         }
         pend = cur;
         rk2 = rk1;
@@ -832,18 +983,171 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     }
     if (pend.r >= 0) {
         if (nobar) collect(P, S, pend, ct);
-        else if (c > 1) settle(P, S, pend, ct, rank);
-        pass_b<OP>(P, S, pend, g, ct, lane, rank);
+        else if (c > 1) settle<OP>(P, S, pend, ct, rank);
+        pass_b<OP>(P, S, pend, g, ct, lane);
     }
     if (kKL && li > 0) {
         named_sync(kBarConsumers, NCT);
-        if (ct == 0) {
-            float L = 0.f;
-            for (int w = 0; w < NCW; ++w) L += S.wl2[(li - 1u) & 1u][w];
-            P.loss[rk1] = L;
-        }
         if (rk2 >= 0) scatter_support(P, S, rk2, (li - 2u) % kSupBufs, ct);
         scatter_support(P, S, rk1, (li - 1u) % kSupBufs, ct);
+    }
+}
+
+// Tail split: the statistics of tail row w.j from every CTA's part of it, merged in CTA
+// order.  Each warp merges on its own (lane i takes parts i, i + 32, ...; a butterfly
+// leaves the same sum in every lane), so every warp of every CTA holding a part gets the
+// same bits.  Waits are bounded like every other wait.
+__device__ void merge_parts(const RowParams& P, Smem& S, Pending& w, int ct, int lane, int U, uint32_t epoch) {
+    const long long G = gridDim.x;
+    const long long TU = (P.ntok - (P.ntok / G) * G) * (long long)U;
+    const long long x0 = w.j * U, x1 = (w.j + 1) * U - 1;
+    const long long b0 = ((x0 + 1) * G - 1) / TU, b1 = ((x1 + 1) * G - 1) / TU;   // CTAs holding units x0, x1
+    MaxSum acc = ms_empty();
+    for (long long b = b0 + lane; b <= b1; b += 32) {
+        const long long lo = b * TU / G;
+        if (lo >= (b + 1) * TU / G) continue;       // a CTA with an empty range holds no part
+        const int which = lo / U == w.j ? 0 : 1;
+        const unsigned int* sl = ws_slot(P, b, which);
+        const long long t0 = clock64();
+        bool ok = true;
+        while (ld_acquire_u32(sl + 2) != epoch) {
+            if (S.abort) { ok = false; break; }
+            if (clock64() - t0 > P.wait_limit) {
+                S.abort = 1;
+                atomicOr(&g_watchdog, 1u);
+                ok = false;
+                break;
+            }
+        }
+        if (!ok) break;
+        float m, sum;
+        asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(m), "=f"(sum) : "l"(sl) : "memory");
+        acc = ms_merge(acc, MaxSum{m, sum});
+    }
+    acc = ms_warp_reduce(acc);
+    w.m = acc.m;
+    w.lnS = logf(acc.s);
+    if (w.first && ct == LT) {
+        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
+        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
+    }
+}
+
+// Self-contained CE with the tail split (one CTA per SM, no clusters): whole rows with
+// the barrier-free statistics of consumer_self, then up to two tail segments whose
+// statistics come from every CTA's part of their row.
+template <int OP>
+__device__ void consumer_split(const RowParams& P, Smem& S) {
+    const int ct = (int)threadIdx.x - 32;
+    const int cw = ct >> 5, lane = ct & 31;
+    const int ncols = (int)P.ncols;
+    const int U = (ncols + 3) >> 2;
+    const uint32_t epoch = ld_relaxed_u32(P.ws) + 1u;
+    // barrier-free statistics need a body tile in every row (the ring then keeps the
+    // warps within kPartBufs rows of each other); shorter rows take the barrier
+    const bool nobar = ncols >= 8;
+    uint32_t g = 0, na = 0, nb = 0;
+    Pending pend;
+    pend.r = -1;
+    Item nxt;
+    bool have = item_at(P, 0, U, nxt);
+    uint32_t nlab = have ? P.labels[nxt.r] : 0u;
+    for (long long i = 0; have; ++i) {
+        const Item it = nxt;
+        const uint32_t lab_r = nlab;
+        have = item_at(P, i + 1, U, nxt);
+        if (have) nlab = P.labels[nxt.r];
+        float* rowp = P.x + it.r * P.ld + P.col0;
+        const Part pt = part_units(rowp, ncols, U, it.u0, it.u1);
+        Pending cur;
+        cur.r = it.r;
+        cur.rowp = rowp;
+        cur.pt = pt;
+        cur.nt = (pt.bn + kTileF - 1) / kTileF;
+        cur.inwin = it.r >= P.ls && it.r < P.le;
+        cur.first = it.u0 == 0;
+        cur.which = it.which;
+        cur.j = it.j;
+        cur.jl = -1;
+        cur.bad = (long long)lab_r >= P.V;
+        if (!cur.bad) {
+            const long long jj = (long long)lab_r - P.col0;
+            if (jj >= pt.lo && jj < pt.hi) cur.jl = (int)jj;
+        }
+        if (cur.bad && cur.inwin && cur.first && ct == LT && P.err) atomicAdd(P.err, 1);
+        cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
+        cur.jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
+        cur.ht = cur.has_ht ? rowp[cur.jht] : 0.f;
+
+        // ---- pass A
+        MaxSum ms = ms_empty();
+        if (cur.has_ht) ms_add(ms, cur.ht);
+        for (int t = 0; t < cur.nt; ++t) {
+            const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
+            wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
+            const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+            float4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int jv = u * NCT + ct;
+                v[u] = jv < n4 ? ld_shared_v4(&S.ring[slot][jv * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
+            ms_addv(ms, v);
+        }
+        g += (uint32_t)cur.nt;
+        ms = ms_warp_reduce(ms);
+        if (it.which < 0 && nobar) {
+            // a whole row: the warps' partials go through the mbarrier buffers
+            cur.ab = na % kPartBufs;
+            cur.apar = (na / kPartBufs) & 1u;
+            ++na;
+            if (lane == 0) {
+                S.wpart[cur.ab][cw] = make_float2(ms.m, ms.s);
+                mbar_arrive(&S.abar[cur.ab]);
+            }
+        } else {
+            const uint32_t b = nb & 1u;
+            ++nb;
+            if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, 0.f, 0.f);
+            named_sync(kBarConsumers, NCT);
+            const MaxSum tot = combine4(S.wred[b], NCW).ms;
+            if (it.which >= 0) {
+                // a tail segment: this CTA's part, published at once for the row's other parts
+                if (ct == 0) publish_part(P, it.which, tot, epoch);
+            } else {
+                cur.m = tot.m;
+                cur.lnS = logf(tot.s);
+                if (ct == LT) {
+                    if (P.lse_out) P.lse_out[it.r] = cur.m + cur.lnS;
+                    if (P.stats_out) { P.stats_out[2 * it.r] = cur.m; P.stats_out[2 * it.r + 1] = cur.lnS; }
+                }
+            }
+        }
+        if (pend.r >= 0) {
+            if (pend.which >= 0) merge_parts(P, S, pend, ct, lane, U, epoch);
+            else if (nobar) collect(P, S, pend, ct);
+            pass_b<OP>(P, S, pend, g, ct, lane);
+        }
+        pend = cur;
+    }
+    if (pend.r >= 0) {
+        if (pend.which >= 0) merge_parts(P, S, pend, ct, lane, U, epoch);
+        else if (nobar) collect(P, S, pend, ct);
+        pass_b<OP>(P, S, pend, g, ct, lane);
+    }
+}
+
+// Tail split: the last CTA to finish advances the workspace generation (every CTA has
+// read it at its start and is done with every slot by now).
+__device__ __forceinline__ void take_ticket(const RowParams& P) {
+    __threadfence();
+    const unsigned int t = atomicAdd(P.ws + 1, 1u);
+    if (t == gridDim.x - 1) {
+        P.ws[1] = 0u;
+        __threadfence();
+        atomicAdd(P.ws, 1u);
     }
 }
 
@@ -875,18 +1179,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
     pdl_wait_primary();
     pdl_launch_dependents();
 
+    const bool split = OP == kCeFused && P.split;
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
-            producer<OP, RES>(P, S, rank, cid, ncl);
-            drain(S);
+            if (split) producer_split(P, S);
+            else producer<OP, RES>(P, S, rank, cid, ncl);
+            drain(S, P.wait_limit);
         }
         __syncwarp();
     } else {
-        if (RES) consumer_self<OP>(P, S, rank, cid, ncl);
+        if (split) consumer_split<OP>(P, S);
+        else if (RES) consumer_self<OP>(P, S, rank, cid, ncl);
         else consumer<OP, false>(P, S, rank, cid, ncl);
     }
     // no CTA may leave while a peer can still write into its shared memory
     if (c > 1) cluster_sync_all();
+    if (split) {
+        __syncthreads();
+        if (threadIdx.x == 0) take_ticket(P);
+    }
 }
 
 const void* kernel_for(int op, bool res) {

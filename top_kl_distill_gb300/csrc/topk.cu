@@ -82,6 +82,7 @@ struct alignas(128) TSmem {
     uint32_t sel[4];
     uint32_t total;                  // candidates held, counted up as warps append
     int need;                        // a warp asks for a cut
+    int nanrow;                      // a NaN was seen in the current row
     int abort;
     uint32_t issued;
 };
@@ -420,6 +421,7 @@ struct RowState {
     bool spec_pending;     // which is set after the first tile
     uint32_t aspec;        // rank, within a warp's share of the first tile, of its estimate
     bool valid_cut;        // a cut over the row's K largest was made
+    bool nan;              // this thread saw a NaN in the row
 };
 
 // Entry of every warp into a collective step.  Returns how many warps had finished the
@@ -455,6 +457,10 @@ __device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[
     for (int u = 0; u < kVecT; ++u) {
         const int j = u * NCT + ct;
         const bool active = j < n4;
+        // a NaN never compares >= T, so it is never admitted; the row is flagged
+        // (the sum is NaN for any NaN member, and for +inf with -inf: then look closer)
+        const float s4 = (v[u].x + v[u].y) + (v[u].z + v[u].w);
+        if (active && s4 != s4) st.nan |= isnan(v[u].x) || isnan(v[u].y) || isnan(v[u].z) || isnan(v[u].w);
         // most float4s hold nothing at or above the threshold: one vote per warp
         const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
         if (__any_sync(0xffffffffu, any)) {
@@ -504,7 +510,7 @@ __device__ __forceinline__ float warp_kth(float4 (&v)[kVecT], uint32_t a, int la
 // Returns false, doing nothing, when the row ran with a speculative threshold that
 // proved too high: fewer than K values at or above it and no exact cut since.
 __device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowState st, long long r, uint32_t* ids,
-                                        float* probs) {
+                                        float* probs, int* err) {
     const int cw = ct >> 5, lane = ct & 31;
     const uint32_t cnt = st.cnt;
     if (st.spec && !st.valid_cut) {
@@ -590,10 +596,13 @@ __device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowS
         }
     }
     named_sync(kBar, NCT);
-    // ---- probabilities renormalised over the k, summed in rank order
-    const float v0 = S.cval[0];
+    // ---- probabilities renormalised over the k, summed in rank order.  A row with fewer
+    //      than K values that are not NaN (NaN is never admitted) fills the rest with
+    //      id 0xFFFFFFFF and probability 0.
+    const uint32_t nout = tot < K ? tot : K;
+    const float v0 = nout ? S.cval[0] : 0.f;
     float part = 0.f;
-    for (uint32_t q = (uint32_t)ct; q < K; q += NCT) part += expf(S.cval[q] - v0);
+    for (uint32_t q = (uint32_t)ct; q < nout; q += NCT) part += expf(S.cval[q] - v0);
     part = warp_sum(part);
     if (lane == 0) S.zred[cw] = part;
     named_sync(kBar, NCT);
@@ -601,19 +610,27 @@ __device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowS
 #pragma unroll
     for (int w = 0; w < NCW; ++w) Z += S.zred[w];
     for (uint32_t q = (uint32_t)ct; q < K; q += NCT) {
-        ids[r * K + q] = S.cid[q];
-        probs[r * K + q] = expf(S.cval[q] - v0) / Z;
+        const bool have = q < nout;
+        ids[r * K + q] = have ? S.cid[q] : 0xFFFFFFFFu;
+        probs[r * K + q] = have ? expf(S.cval[q] - v0) / Z : 0.f;
     }
     for (int i = ct; i < NBC; i += NCT) S.hcnt[i] = 0u;
-    if (ct == 0) { S.total = 0; S.need = 0; }
-    named_sync(kBar, NCT);   // the regions, S.zred and S.total are reused by the next row
+    if (ct == 0) {
+        S.total = 0;
+        S.need = 0;
+        if (S.nanrow) {                       // one count per row that holds a NaN
+            if (err) atomicAdd(err, 1);
+            S.nanrow = 0;
+        }
+    }
+    named_sync(kBar, NCT);   // the regions, S.zred, S.total and S.nanrow are reused by the next row
     return true;
 }
 
 // ---------------------------------------------------------------- consumer
 
 __device__ void consumer(const float* x, long long ld, long long V, int k, long long ls, long long le,
-                         uint32_t* ids, float* probs, TSmem& S) {
+                         uint32_t* ids, float* probs, int* err, TSmem& S) {
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
     const uint32_t K = (uint32_t)k;
@@ -639,6 +656,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         st.T = -INFINITY;
         st.adm = 0;
         st.valid_cut = false;
+        st.nan = false;
         {
             // a warp's share of the first tile holds K * (kTileT / NCW) / V of the row's
             // K largest on average; its estimate is the value with 1.4 times that many (at
@@ -660,6 +678,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
                 uint32_t id = 0;
                 if (ct < h) { id = (uint32_t)ct; v = rowp[id]; keep = true; }
                 else if (ct >= 4 && ct - 4 < (int)V - t0) { id = (uint32_t)(t0 + ct - 4); v = rowp[id]; keep = true; }
+                if (keep && isnan(v)) { keep = false; st.nan = true; }
                 wappend(S, cw, st.cnt, keep, v, id);
             }
         };
@@ -718,9 +737,10 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         }
         g += (uint32_t)nt;
         if (lane == 0) S.wadm[cw] = st.adm;
+        if (st.nan) S.nanrow = 1;
         while (collective(S, st, K, limit, ct, true) != (uint32_t)NCW) {
         }
-        if (finish_row(S, K, ct, st, r, ids, probs)) continue;
+        if (finish_row(S, K, ct, st, r, ids, probs, err)) continue;
 
         // ---- the speculative threshold was too high: the row again, exactly, read from
         //      global memory (the ring has moved on to the next rows)
@@ -730,6 +750,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
         st.spec = false;
         st.spec_pending = false;
         st.valid_cut = false;
+        st.nan = false;
         head_tail();
         for (int t = 0; t < nt; ++t) {
             if (__shfl_sync(0xffffffffu, *need, 0) || st.cnt + PER_TILE > (uint32_t)RW) {
@@ -746,15 +767,16 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
             }
             admit(S, st, v, n4, h, t, ct, trig);
         }
+        if (st.nan) S.nanrow = 1;
         while (collective(S, st, K, limit, ct, true) != (uint32_t)NCW) {
         }
-        finish_row(S, K, ct, st, r, ids, probs);
+        finish_row(S, K, ct, st, r, ids, probs, err);
     }
 }
 
 __global__ void __maxnreg__(128)
 topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long long ls, long long le,
-            uint32_t* __restrict__ ids, float* __restrict__ probs) {
+            uint32_t* __restrict__ ids, float* __restrict__ probs, int* err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     TSmem& S = *reinterpret_cast<TSmem*>(smem_raw);
     if (threadIdx.x == 0) {
@@ -766,6 +788,7 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
         S.issued = 0;
         S.total = 0;
         S.need = 0;
+        S.nanrow = 0;
         fence_mbar_init_cluster();
     }
     for (int i = (int)threadIdx.x; i < NBC; i += (int)blockDim.x) S.hcnt[i] = 0u;
@@ -781,7 +804,7 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
         }
         __syncwarp();
     } else {
-        consumer(x, ld, V, k, ls, le, ids, probs, S);
+        consumer(x, ld, V, k, ls, le, ids, probs, err, S);
     }
 }
 
@@ -791,7 +814,6 @@ std::atomic<int> g_attr_done[64];
 
 cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long V, int k, long long ls,
                         long long le, uint32_t* ids, float* probs, int* err, cudaStream_t st) {
-    (void)err;
     (void)ntok;
     if (k < 1 || k > KMAXT) return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
@@ -824,7 +846,7 @@ cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_kernel, x, ld, V, k, ls, le, ids, probs);
+    return cudaLaunchKernelEx(&cfg, topk_kernel, x, ld, V, k, ls, le, ids, probs, err);
 }
 
 unsigned int topk_watchdog(bool clear) {

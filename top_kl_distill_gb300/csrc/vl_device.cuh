@@ -78,7 +78,7 @@ constexpr long long kWaitTimeoutCycles = 4000000000ll;
 // abort flag are only read after many failed polls.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                            unsigned int* flag) {
+                                            unsigned int* flag, long long limit = kWaitTimeoutCycles) {
     const uint32_t b = smem_u32(bar);
     long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -88,7 +88,7 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, vola
             const long long now = clock64();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitTimeoutCycles) {
+            } else if (now - t0 > limit) {
                 *abort = 1;
                 atomicOr(flag, 1u);
                 return false;
@@ -98,11 +98,12 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity, vola
 }
 
 // Same wait without the abort check, for draining copies already in flight.
-__device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_parity_drain(uint64_t* bar, uint32_t parity,
+                                                  long long limit = kWaitTimeoutCycles) {
     const uint32_t b = smem_u32(bar);
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (clock64() - t0 > kWaitTimeoutCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }
@@ -184,6 +185,11 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
 __device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
                  :: "r"(addr), "f"(a), "f"(b), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar) {

@@ -21,11 +21,21 @@ struct RowParams {
     const float* lse_in;      // given row statistics (stats_in wins)
     const float* stats_in;
     float* loss;              // per-row loss (CE loss / KL / CE loss part)
+    float* ce_loss;           // self-contained KL with labels: the CE loss of the row as well (nullable)
     float* lse_out;
     float* stats_out;
     int* err;
     int csize;                // CTAs per row (cluster size)
+    long long wait_limit;     // SM cycles after which a wait gives up (normally about 2 s)
+    long long withhold;       // test hook: body tile of CTA 0 the producer never issues (-1: none)
+    unsigned int* ws;         // tail split (CE fused): exchange workspace, see rows.cu
+    int split;                // 1: the rows past the last full wave are split over all CTAs
 };
+
+// Exchange workspace of the tail split: a header (generation, ticket) and one 16-byte
+// slot per (CTA, tail segment).
+constexpr int kWsHeaderWords = 4;
+constexpr long long ws_bytes_for(long long ctas) { return 4LL * kWsHeaderWords + 32LL * ctas; }
 
 enum RowOp : int { kCeFused = 0, kCeFwd = 1, kCeBwd = 2, kKl = 3 };
 

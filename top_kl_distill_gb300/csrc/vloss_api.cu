@@ -34,11 +34,13 @@ vl_status ok() { return VL_OK; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-constexpr long long kMaxCols = 0x7fffffffLL;   // ids and labels are uint32 columns
+// Longest row: the kernels index a row with 32-bit ints and step through it in
+// tiles of a few thousand columns, so a row stays 2^16 columns short of 2^31.
+constexpr long long kMaxCols = VL_MAX_COLS;
 
 vl_status check_rows(const void* logits, int64_t ld, int64_t ntok, int64_t V, const char* fn) {
     if (ntok < 0) return fail(VL_EINVAL, "%s: ntok < 0", fn);
-    if (V < 1 || V > kMaxCols) return fail(VL_EINVAL, "%s: V must be in [1, 2^31)", fn);
+    if (V < 1 || V > kMaxCols) return fail(VL_EINVAL, "%s: V must be in [1, %lld]", fn, kMaxCols);
     if (ld < V) return fail(VL_EINVAL, "%s: ld (%lld) < V (%lld)", fn, (long long)ld, (long long)V);
     if (ntok > 0 && logits == nullptr) return fail(VL_EINVAL, "%s: logits is NULL", fn);
     return ok();
@@ -81,17 +83,32 @@ struct Grid {
     int nclusters;
 };
 
+int l2_bytes() {
+    static std::atomic<int> cache[64];
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_acquire);
+        if (c > 0) return c;
+    }
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_release);
+    return v;
+}
+
 Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
     const int sms = num_sms();
     if (!resident) {
         long long g = rows < sms ? rows : sms;
         return Grid{1, (int)(g > 0 ? g : 1)};
     }
-    // the KL loss of a row is reduced inside one CTA: no cluster split
-    if (op == kKl) {
-        long long g = rows < sms ? rows : sms;
-        return Grid{1, (int)(g > 0 ? g : 1)};
-    }
+    // Self-contained mode re-reads a row part in pass B from L2 while the next part is
+    // read: about two parts of 4 ncols / c bytes per CTA are live.  Splitting a row over
+    // c CTAs keeps them within a third of L2 (c = 4 at 128256 columns on a GB300).
+    const double live = 2.0 * 4.0 * (double)ncols * (double)sms;
+    const double budget = l2_bytes() > 0 ? l2_bytes() / 3.0 : 40e6;
+    int cmin = 1;
+    while (cmin < kMaxCluster && live / cmin > budget) ++cmin;
     static const int forced = [] {
         const char* e = std::getenv("VLOSS_CLUSTER");
         return e ? std::atoi(e) : 0;
@@ -103,7 +120,7 @@ Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
     const double exchange = 4.0 * kTileF;
     Grid best{0, 0};
     double best_cost = 0;
-    for (int c = 1; c <= kMaxCluster; ++c) {
+    for (int c = cmin; c <= kMaxCluster; ++c) {
         const int n = row_max_clusters(op, resident, c);
         if (n <= 0) continue;
         const long long ncl = rows < n ? rows : n;
@@ -223,14 +240,42 @@ RowParams base_params(float* logits, int64_t ld, int64_t ntok, int64_t V) {
     P.col0 = 0;
     P.ncols = V;
     P.csize = 1;
+    P.wait_limit = kWaitTimeoutCycles;
+    P.withhold = -1;
     return P;
 }
+
+// Test hook (vl_test_inject_wait_timeout): applies to the next row-engine launch made
+// from this host thread, then clears itself.
+thread_local long long g_inject_withhold = -1;
+thread_local long long g_inject_wait = 0;
 
 vl_status run_rows(int op, bool resident, RowParams& P, long long rows, const char* fn, cudaStream_t st) {
     const Grid g = choose_grid(op, resident, rows, P.ncols);
     if (g.csize == 0) return fail(VL_ELAUNCH, "%s: no launch configuration fits this device", fn);
     P.csize = g.csize;
+    if (g_inject_wait > 0) {
+        P.withhold = g_inject_withhold;
+        P.wait_limit = g_inject_wait;
+        g_inject_withhold = -1;
+        g_inject_wait = 0;
+    }
     const cudaError_t e = launch_rows(op, resident, P, g.nclusters, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+// The tail-split launch of the fused CE kernel: one CTA per SM.
+vl_status run_split(RowParams& P, int sms, const char* fn, cudaStream_t st) {
+    if (row_max_clusters(kCeFused, true, 1) <= 0) return fail(VL_ELAUNCH, "%s: the row kernel does not fit", fn);
+    P.csize = 1;
+    if (g_inject_wait > 0) {
+        P.withhold = g_inject_withhold;
+        P.wait_limit = g_inject_wait;
+        g_inject_withhold = -1;
+        g_inject_wait = 0;
+    }
+    const cudaError_t e = launch_rows(kCeFused, true, P, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
 }
@@ -311,14 +356,31 @@ vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, 
 
 vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
                       int64_t loss_start, int64_t loss_end, float scale, float* loss, float* lse, float* stats,
-                      float* mean, int32_t* err, void* stream) {
+                      float* mean, int32_t* err, void* workspace, void* stream) {
     const char* fn = "vl_ce_fused";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
     if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return fail(VL_EINVAL, "%s: workspace not 16-byte aligned", fn);
     const cudaStream_t st = as_stream(stream);
-    if (ntok > 0) {
+    const int sms = num_sms();
+    // the tail split pays off when the rows do not fill whole waves of the SMs
+    if (ntok > 0 && workspace && sms > 0 && ntok % sms != 0 && ws_bytes_for(sms) <= VL_WORKSPACE_BYTES) {
+        RowParams P = base_params(logits, ld, ntok, V);
+        P.labels = labels;
+        P.ls = loss_start;
+        P.le = loss_end;
+        P.cg = scale;
+        P.ce_coef = scale;
+        P.loss = loss;
+        P.lse_out = lse;
+        P.stats_out = stats;
+        P.err = err;
+        P.ws = static_cast<unsigned int*>(workspace);
+        P.split = 1;
+        if ((s = run_split(P, sms, fn, st))) return s;
+    } else if (ntok > 0) {
         RowParams P = base_params(logits, ld, ntok, V);
         P.labels = labels;
         P.ls = loss_start;
@@ -376,6 +438,46 @@ vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
     return run_rows(kKl, self, P, rows > 0 ? rows : 1, fn, as_stream(stream));
 }
 
+vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                         const uint32_t* tid, const float* tp, int64_t k, float coef, float ce_coef,
+                         int64_t loss_start, int64_t loss_end, float* kl_loss, float* ce_loss, float* lse,
+                         float* stats, float* ce_mean, int32_t* err, void* stream) {
+    const char* fn = "vl_ce_kl_fused";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (k < 1) return fail(VL_EINVAL, "%s: k < 1", fn);
+    if (k > VL_KL_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_KL_KMAX);
+    if (ntok > 0 && (labels == nullptr || tid == nullptr || tp == nullptr || kl_loss == nullptr ||
+                     ce_loss == nullptr))
+        return fail(VL_EINVAL, "%s: labels, tid, tp, kl_loss or ce_loss is NULL", fn);
+    const cudaStream_t st = as_stream(stream);
+    if (ntok > 0) {
+        RowParams P = base_params(logits, ld, ntok, V);
+        P.tid = tid;
+        P.tp = tp;
+        P.k = (int)k;
+        P.labels = labels;
+        P.coef = coef;
+        P.ce_coef = ce_coef;
+        P.cg = coef + ce_coef;
+        P.ls = loss_start;
+        P.le = loss_end;
+        P.loss = kl_loss;
+        P.ce_loss = ce_loss;
+        P.lse_out = lse;
+        P.stats_out = stats;
+        P.err = err;
+        const long long rows = loss_end - loss_start;
+        if ((s = run_rows(kKl, true, P, rows > 0 ? rows : 1, fn, st))) return s;
+    }
+    if (ce_mean) {
+        const cudaError_t e = launch_mean(ce_loss, loss_start, loss_end, ce_mean, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return VL_OK;
+}
+
 vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k, int64_t loss_start,
                        int64_t loss_end, uint32_t* ids, float* probs, int32_t* err, void* stream) {
     const char* fn = "vl_topk_rows";
@@ -389,6 +491,19 @@ vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V,
     if (loss_end == loss_start) return VL_OK;
     const cudaError_t e = launch_topk(logits, ld, ntok, V, (int)k, loss_start, loss_end, ids, probs, err,
                                       as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
+vl_status vl_window_mean(const float* loss, int64_t ntok, int64_t loss_start, int64_t loss_end, float* mean,
+                         void* stream) {
+    const char* fn = "vl_window_mean";
+    if (ntok < 0) return fail(VL_EINVAL, "%s: ntok < 0", fn);
+    vl_status s = check_window(loss_start, loss_end, ntok, fn);
+    if (s) return s;
+    if (mean == nullptr) return fail(VL_EINVAL, "%s: mean is NULL", fn);
+    if (loss_end > loss_start && loss == nullptr) return fail(VL_EINVAL, "%s: loss is NULL", fn);
+    const cudaError_t e = launch_mean(loss, loss_start, loss_end, mean, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return VL_OK;
 }
@@ -420,6 +535,15 @@ vl_status vl_acc_add(float* a, const float* b, int64_t n, void* stream) {
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
+vl_status vl_test_inject_wait_timeout(int64_t withhold_tile, int64_t wait_cycles) {
+    if (withhold_tile < 0 || wait_cycles < 1000 || wait_cycles > kWaitTimeoutCycles)
+        return fail(VL_EINVAL, "vl_test_inject_wait_timeout: need withhold_tile >= 0 and wait_cycles in [1000, %lld]",
+                    (long long)kWaitTimeoutCycles);
+    g_inject_withhold = withhold_tile;
+    g_inject_wait = wait_cycles;
     return VL_OK;
 }
 

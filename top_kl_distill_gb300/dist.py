@@ -3,8 +3,10 @@
 One process per GPU (torchrun sets RANK, LOCAL_RANK, WORLD_SIZE).  Rows are
 independent units -- every per-row output (loss, lse, gradient row, top-k)
 depends on its own row only -- so a batch is split into contiguous row shards
-and no collective touches the data path.  The only cross-rank step is the
-reduction of a scalar (the slowest rank's time, or a loss sum) on the host side.
+and no collective touches the per-row data.  The one exchange step is the mean
+over the loss window, which spans the shards: each rank takes the mean over its
+part of the window (vl_window_mean, or the mean output of the loss call) and one
+all-reduce of mean x count gives the batch's mean.
 """
 from __future__ import annotations
 
@@ -35,3 +37,30 @@ def max_over_ranks(value: float, device: str = "cuda") -> float:
     t = torch.tensor([float(value)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t[0])
+
+
+def window_shard(ntok: int, rank: int, ws: int, loss_start: int, loss_end: int) -> tuple[int, int, int, int]:
+    """Rows [r0, r1) of rank `rank` and the part of the loss window [loss_start, loss_end)
+    that falls inside them, relative to r0 (an empty window when none does)."""
+    if not 0 <= loss_start <= loss_end <= ntok:
+        raise ValueError(f"window [{loss_start}, {loss_end}) not inside [0, {ntok}]")
+    r0, r1 = shard(ntok, rank, ws)
+    ls = min(max(loss_start - r0, 0), r1 - r0)
+    le = min(max(loss_end - r0, 0), r1 - r0)
+    return r0, r1, ls, le
+
+
+def global_window_mean(local_mean, local_count: int, total_count: int):
+    """The mean over the whole loss window from this rank's mean over its part of it
+    (a one-element tensor) and that part's row count: one all-reduce (sum) of
+    local_mean x local_count in float64, divided by the window's total row count; 0 for
+    an empty window, as the page's read_loss gives.  Returns a float64 one-element
+    tensor on local_mean's device, the same on every rank."""
+    import torch
+    import torch.distributed as dist
+    t = local_mean.detach().reshape(1).to(torch.float64) * float(local_count)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    if total_count <= 0:
+        return torch.zeros_like(t)
+    return t / float(total_count)

@@ -23,6 +23,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "vloss.h")
 VL_OK, VL_EINVAL, VL_ELAUNCH, VL_EUNSUPPORTED = 0, 1, 2, 3
 VL_KL_KMAX = 1024
 VL_TOPK_KMAX = 2048
+VL_MAX_COLS = 0x7FFF0000
+VL_WORKSPACE_BYTES = 65536
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int64
@@ -31,10 +33,13 @@ _F = ctypes.c_float
 _SIGS = {
     "vl_ce_fwd": [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P],
     "vl_ce_bwd_inplace": [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P],
-    "vl_ce_fused": [_P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _P, _P, _P, _P],
+    "vl_ce_fused": [_P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P],
     "vl_kl_topk_inplace": [_P, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _I, _P, _P, _P, _F, _P, _P, _P],
     "vl_topk_rows": [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P],
+    "vl_ce_kl_fused": [_P, _I, _I, _I, _P, _P, _P, _I, _F, _F, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "vl_acc_add": [_P, _P, _I, _P],
+    "vl_test_inject_wait_timeout": [_I, _I],
+    "vl_window_mean": [_P, _I, _I, _I, _P, _P],
 }
 
 _lib = None
@@ -127,12 +132,42 @@ def vl_ce_bwd_inplace(logits, ld, ntok, V, col0, ncols, labels, lse, stats, loss
         _ptr(loss_part, "f32", "loss_part"), _ptr(err, "i32", "err"), _stream(stream)))
 
 
+_workspaces = {}
+
+
+def workspace(device=None):
+    """The binding's exchange workspace for vl_ce_fused on `device` (VL_WORKSPACE_BYTES,
+    zero-filled once).  One per device: calls that use it must not overlap on the GPU;
+    give concurrent streams workspaces of their own."""
+    import torch
+    dev = torch.cuda.current_device() if device is None else int(device)
+    ws = _workspaces.get(dev)
+    if ws is None:
+        ws = torch.zeros(VL_WORKSPACE_BYTES, dtype=torch.uint8, device=f"cuda:{dev}")
+        _workspaces[dev] = ws
+    return ws
+
+
+def _ws(w, logits):
+    if isinstance(w, str):
+        if w != "auto":
+            raise ValueError("workspace: a tensor, an int address, None or 'auto'")
+        import torch
+        dev = logits.device.index if isinstance(logits, torch.Tensor) else None
+        return workspace(dev).data_ptr()
+    if w is None or isinstance(w, int):
+        return w
+    if w.numel() * w.element_size() < VL_WORKSPACE_BYTES or not w.is_cuda:
+        raise ValueError(f"workspace: need {VL_WORKSPACE_BYTES} bytes of device memory")
+    return w.data_ptr()
+
+
 def vl_ce_fused(logits, ld, ntok, V, labels, loss_start, loss_end, scale, loss, lse=None, stats=None,
-                mean=None, err=None, stream=None):
+                mean=None, err=None, workspace="auto", stream=None):
     _check("vl_ce_fused", lib().vl_ce_fused(
         _ptr(logits, "f32", "logits"), ld, ntok, V, _ptr(labels, "u32", "labels"), loss_start, loss_end,
         float(scale), _ptr(loss, "f32", "loss"), _ptr(lse, "f32", "lse"), _ptr(stats, "f32", "stats"),
-        _ptr(mean, "f32", "mean"), _ptr(err, "i32", "err"), _stream(stream)))
+        _ptr(mean, "f32", "mean"), _ptr(err, "i32", "err"), _ws(workspace, logits), _stream(stream)))
 
 
 def vl_kl_topk_inplace(logits, ld, ntok, V, col0, ncols, tid, tp, k, coef, loss_start, loss_end,
@@ -144,14 +179,33 @@ def vl_kl_topk_inplace(logits, ld, ntok, V, col0, ncols, tid, tp, k, coef, loss_
         _stream(stream)))
 
 
+def vl_ce_kl_fused(logits, ld, ntok, V, labels, tid, tp, k, coef, ce_coef, loss_start, loss_end, kl_loss,
+                   ce_loss, lse=None, stats=None, ce_mean=None, err=None, stream=None):
+    _check("vl_ce_kl_fused", lib().vl_ce_kl_fused(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, _ptr(labels, "u32", "labels"), _ptr(tid, "u32", "tid"),
+        _ptr(tp, "f32", "tp"), k, float(coef), float(ce_coef), loss_start, loss_end,
+        _ptr(kl_loss, "f32", "kl_loss"), _ptr(ce_loss, "f32", "ce_loss"), _ptr(lse, "f32", "lse"),
+        _ptr(stats, "f32", "stats"), _ptr(ce_mean, "f32", "ce_mean"), _ptr(err, "i32", "err"),
+        _stream(stream)))
+
+
 def vl_topk_rows(logits, ld, ntok, V, k, loss_start, loss_end, ids, probs, err=None, stream=None):
     _check("vl_topk_rows", lib().vl_topk_rows(
         _ptr(logits, "f32", "logits"), ld, ntok, V, k, loss_start, loss_end, _ptr(ids, "u32", "ids"),
         _ptr(probs, "f32", "probs"), _ptr(err, "i32", "err"), _stream(stream)))
 
 
+def vl_window_mean(loss, ntok, loss_start, loss_end, mean, stream=None):
+    _check("vl_window_mean", lib().vl_window_mean(_ptr(loss, "f32", "loss"), ntok, loss_start, loss_end,
+                                                  _ptr(mean, "f32", "mean"), _stream(stream)))
+
+
 def vl_acc_add(a, b, n, stream=None):
     _check("vl_acc_add", lib().vl_acc_add(_ptr(a, "f32", "a"), _ptr(b, "f32", "b"), n, _stream(stream)))
+
+
+def vl_test_inject_wait_timeout(withhold_tile: int, wait_cycles: int):
+    _check("vl_test_inject_wait_timeout", lib().vl_test_inject_wait_timeout(withhold_tile, wait_cycles))
 
 
 def vl_watchdog_flag(device: int = 0, clear: bool = True) -> int:
