@@ -181,6 +181,28 @@ class CeFused(Case):
         self.step(j, mean=False)
 
 
+class CeFusedBf16(CeFused):
+    """The fused CE step on bf16 logits (the same draws rounded to bf16): vl_ce_fused_bf16,
+    2 bytes an element each way."""
+
+    def __init__(self, torch, w, nbuf):
+        super().__init__(torch, w, nbuf)
+        self.name = w.name + "_bf16"
+        self.pristine = self.pristine.to(torch.bfloat16)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+
+    def bytes_per_step(self):
+        return self.w.ntok * (4 * self.w.V + 12) + (self.w.loss_end - self.w.loss_start) * 4 + 4
+
+    def kernel_bytes(self):
+        return self.w.ntok * (4 * self.w.V + 12)
+
+    def step(self, j, mean=True):
+        w = self.w
+        self.vl.vl_ce_fused_bf16(self.bufs[j], w.V, w.ntok, w.V, self.labels, w.loss_start, w.loss_end, w.scale,
+                                 self.loss, self.lse, None, self.mean if mean else None, None)
+
+
 class Kl(Case):
     def __init__(self, torch, w, nbuf):
         from top_kl_distill_gb300 import vloss as vl
@@ -227,6 +249,7 @@ class TopK(Case):
         self.bufs = [self.x]
         self.ids = torch.zeros((w.ntok, k), dtype=torch.int32, device="cuda")
         self.probs = torch.zeros((w.ntok, k), device="cuda")
+        self.launches_per_step = 3 if vl.vl_topk_workspace_bytes(w.ntok, w.V, k) else 1
 
     def rows(self):
         return self.w.ntok
@@ -240,6 +263,8 @@ class TopK(Case):
         pass
 
     def step(self, j):
+        """One vl_topk_rows call: with the workspace, the filter, finish and exact-rows
+        kernels (the last one finds its list empty on these rows)."""
         w = self.w
         self.vl.vl_topk_rows(self.x, w.V, w.ntok, w.V, self.k, 0, w.ntok, self.ids, self.probs)
 
@@ -290,6 +315,30 @@ class LargeV(Case):
 
     def kernel(self, j):
         self.step(j, mean=False)
+
+
+class LargeVBf16(LargeV):
+    """The one-pass large-vocabulary step on bf16 logits (vl_ce_kl_fused_bf16)."""
+
+    def __init__(self, torch, w, nbuf):
+        super().__init__(torch, w, nbuf)
+        self.name = w.name + "_bf16"
+        self.pristine = self.pristine.to(torch.bfloat16)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+
+    def bytes_per_step(self):
+        w = self.w
+        return w.ntok * (4 * w.V + 8 * w.k + 4 + 8) + (w.loss_end - w.loss_start) * 4 + 4
+
+    def kernel_bytes(self):
+        w = self.w
+        return w.ntok * (4 * w.V + 8 * w.k + 4 + 8)
+
+    def step(self, j, mean=True):
+        w = self.w
+        self.vl.vl_ce_kl_fused_bf16(self.bufs[j], w.V, w.ntok, w.V, self.labels, self.tid, self.tp, w.k, w.coef,
+                                    w.ce_coef, w.loss_start, w.loss_end, self.kl_loss, self.ce_loss, None, None,
+                                    self.mean if mean else None, None)
 
 
 class LargeVSliced(Case):
@@ -359,7 +408,10 @@ def nbuf_for(bytes_per_buf: int) -> int:
 def base_workload(name):
     if name.startswith("topk"):
         return W.WORKLOADS[name.split("_k")[0]]
-    return W.WORKLOADS[name[:-len("_sliced")] if name.endswith("_sliced") else name]
+    for suffix in ("_sliced", "_bf16"):
+        if name.endswith(suffix):
+            return W.WORKLOADS[name[:-len(suffix)]]
+    return W.WORKLOADS[name]
 
 
 def make_case(torch, name, ntok=None, nbuf=None):
@@ -368,14 +420,16 @@ def make_case(torch, name, ntok=None, nbuf=None):
         w = w.scaled(ntok)
     nb = nbuf or nbuf_for(w.ntok * w.V * 4)
     if w.kind == "ce":
-        return CeFused(torch, w, nb)
+        return CeFusedBf16(torch, w, nb) if name.endswith("_bf16") else CeFused(torch, w, nb)
     if w.kind == "kl":
         return Kl(torch, w, nb)
     if w.kind == "topk":
         k = int(name.split("_k")[1]) if "_k" in name else w.k
         return TopK(torch, w, 1, k)
     if w.kind == "ce_kl_sliced":
-        return LargeVSliced(torch, w, nb) if name.endswith("_sliced") else LargeV(torch, w, nb)
+        if name.endswith("_sliced"):
+            return LargeVSliced(torch, w, nb)
+        return LargeVBf16(torch, w, nb) if name.endswith("_bf16") else LargeV(torch, w, nb)
     raise ValueError(name)
 
 
@@ -455,7 +509,7 @@ def e2e_ce(torch, case, steps, warmup, chunks=4, nstreams=2):
     The batch goes in row chunks over `nstreams` streams, so that the upload of one
     chunk, the fused call on another and the download of a third overlap: per chunk,
     H2D of its logits and labels, vl_ce_fused over its rows (window clipped to them,
-    the batch's scale; a workspace per stream), D2H of its gradient, loss and lse.
+    the batch's scale), D2H of its gradient, loss and lse.
     Then vl_window_mean over the whole window and D2H of the mean.  All of it is inside
     the timed region.  Returns (ms per step, H2D bytes, D2H bytes)."""
     w, vl = case.w, case.vl
@@ -468,7 +522,6 @@ def e2e_ce(torch, case, steps, warmup, chunks=4, nstreams=2):
     hmean = torch.empty(1).pin_memory()
     x, lab = case.bufs[0], case.labels
     streams = [torch.cuda.Stream() for _ in range(nstreams)]
-    wss = [torch.zeros(vl.VL_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda") for _ in range(nstreams)]
     spans = [(i * n // chunks, (i + 1) * n // chunks) for i in range(chunks)]
     main = torch.cuda.current_stream()
 
@@ -484,7 +537,7 @@ def e2e_ce(torch, case, steps, warmup, chunks=4, nstreams=2):
                 ls = min(max(w.loss_start - r0, 0), r1 - r0)
                 le = min(max(w.loss_end - r0, 0), r1 - r0)
                 vl.vl_ce_fused(x[r0:r1], V, r1 - r0, V, lab[r0:r1], ls, le, w.scale, case.loss[r0:r1],
-                               case.lse[r0:r1], None, None, None, wss[i % nstreams], st)
+                               case.lse[r0:r1], None, None, None, st)
                 hg[r0:r1].copy_(x[r0:r1], non_blocking=True)
                 hloss[r0:r1].copy_(case.loss[r0:r1], non_blocking=True)
                 hlse[r0:r1].copy_(case.lse[r0:r1], non_blocking=True)
@@ -543,7 +596,7 @@ def roofline(case, kernel_ms, peak, peak_kind, tag):
 
 
 KERNEL_TAG = {"ce_lm": "ce_fused", "ce_tiny": "ce_fused_tiny", "kl": "kl_resident", "large_v": "ce_kl_fused",
-              "large_v_sliced": "kl_sliced_stream"}
+              "large_v_sliced": "kl_sliced_stream", "ce_lm_bf16": "ce_fused_bf16", "large_v_bf16": "ce_kl_fused_bf16"}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
@@ -821,7 +874,8 @@ def main():
 
     if not args.no_sweep:
         sweep = {}
-        names = ["ce_tiny", "kl", "topk_k256", "topk_k2048", "large_v", "large_v_sliced"]
+        names = ["ce_tiny", "ce_lm_bf16", "kl", "topk_k256", "topk_k2048", "large_v", "large_v_bf16",
+                 "large_v_sliced"]
         if args.sweep_only:
             names = [n for n in args.sweep_only.split(",") if n]
         for name in names:

@@ -70,7 +70,6 @@ typedef enum vl_status {
 #define VL_KL_KMAX 1024      /* teacher support per row for vl_kl_topk_inplace */
 #define VL_TOPK_KMAX 2048    /* k of vl_topk_rows (the page's bound for topk_rows) */
 #define VL_MAX_COLS 0x7FFF0000LL   /* longest row V (2^31 - 2^16): rows are indexed with 32-bit ints */
-#define VL_WORKSPACE_BYTES 65536   /* size of the optional exchange workspace of vl_ce_fused */
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 VL_API int vl_version(void);
@@ -118,20 +117,11 @@ VL_API vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int6
  * Cross-entropy forward and backward in one pass over each row: the row is read from
  * HBM once and the gradient written once.  Outputs as vl_ce_fwd, then logits rows are
  * overwritten as vl_ce_bwd_inplace does with col0 = 0, ncols = V.
- *   workspace (nullable): VL_WORKSPACE_BYTES bytes of device memory owned by the caller,
- *     16-byte aligned and zero-filled before its first use.  With it, when the rows do
- *     not divide evenly among the SMs, the rows left over after the last full wave are
- *     cut into equal column ranges across all SMs (the parts exchange their row
- *     statistics through the workspace), so no SM carries a whole extra row; results
- *     are the same either way up to fp32 rounding.  Without it (NULL) a row stays on
- *     one SM or one thread-block cluster.  Every call leaves the workspace ready for the
- *     next one; calls that share a workspace must not overlap on the GPU (use one per
- *     stream), or they race.
  */
 VL_API vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V,
                       const uint32_t* labels, int64_t loss_start, int64_t loss_end,
                       float scale, float* loss, float* lse, float* stats, float* mean,
-                      int32_t* err, void* workspace, void* stream);
+                      int32_t* err, void* stream);
 
 /*
  * Top-k distillation KL with the gradient written in place (train_head.rs: module doc,
@@ -184,6 +174,41 @@ VL_API vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t
                          int32_t* err, void* stream);
 
 /*
+ * bf16 logits (the page keeps f16 activations beside f32 logits, train_head.rs: Head,
+ * head_kl's cvt / cvt_cols): the same five calls over rows of bf16 logits, given as
+ * their 16-bit patterns (the upper half of an fp32).  Each row is read as bf16, every
+ * maximum, sum, logarithm and exponential is taken in fp32, and each gradient element
+ * is rounded to bf16 (nearest even) once, when it is written in place; losses, lse and
+ * stats are fp32 as above.  Arguments, outputs and errors as in the fp32 calls; rows
+ * may start at any 2-byte boundary, with any ld >= V.  Half the bytes of a row per pass.
+ */
+VL_API vl_status vl_ce_fwd_bf16(const uint16_t* logits, int64_t ld, int64_t ntok, int64_t V,
+                    const uint32_t* labels, int64_t loss_start, int64_t loss_end,
+                    float* loss, float* lse, float* stats, float* mean,
+                    int32_t* err, void* stream);
+VL_API vl_status vl_ce_bwd_inplace_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V,
+                            int64_t col0, int64_t ncols, const uint32_t* labels,
+                            const float* lse, const float* stats,
+                            int64_t loss_start, int64_t loss_end, float scale,
+                            float* loss_part, int32_t* err, void* stream);
+VL_API vl_status vl_ce_fused_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V,
+                      const uint32_t* labels, int64_t loss_start, int64_t loss_end,
+                      float scale, float* loss, float* lse, float* stats, float* mean,
+                      int32_t* err, void* stream);
+VL_API vl_status vl_kl_topk_inplace_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V,
+                             int64_t col0, int64_t ncols,
+                             const uint32_t* tid, const float* tp, int64_t k, float coef,
+                             int64_t loss_start, int64_t loss_end,
+                             const float* lse_in, const float* stats_in,
+                             const uint32_t* labels, float ce_coef,
+                             float* loss, int32_t* err, void* stream);
+VL_API vl_status vl_ce_kl_fused_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V,
+                         const uint32_t* labels, const uint32_t* tid, const float* tp, int64_t k,
+                         float coef, float ce_coef, int64_t loss_start, int64_t loss_end,
+                         float* kl_loss, float* ce_loss, float* lse, float* stats, float* ce_mean,
+                         int32_t* err, void* stream);
+
+/*
  * Teacher top-k per row (train_head.rs: topk_rows): ids[t][q], q < k, are the columns of
  * the k largest logits of row t in descending order of value, ties broken by the lower
  * column (-0.0 equals +0.0); probs[t][q] = exp(s[ids[q]] - s[ids[0]]) / sum over the k.
@@ -196,10 +221,30 @@ VL_API vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t
  * first 3840 columns, and a row for which fewer than k values reach it (one sorted in
  * descending order, for instance) is read a second time; the result is exact either way.
  *   ids [ntok][k] u32, probs [ntok][k] fp32, err: one int32 counter (nullable).
+ *   workspace (nullable), workspace_bytes: device memory owned by the caller, 16-byte
+ *     aligned, no initial contents needed.  Rows of 30720 to 2^20 columns with k up to
+ *     about 6% of V are then streamed by one kernel whose filter warps write each row's
+ *     candidates to the workspace while its finish warps order the previous row; the rare
+ *     row it cannot settle goes to the exact kernel.  vl_topk_workspace_bytes gives the
+ *     size for one CTA per SM of the current device; a smaller workspace that still holds
+ *     one CTA's candidate regions runs fewer CTAs, and one below that (or none) has each
+ *     row selected and ordered by the single exact kernel.  Same results either way.
+ *     Calls that share a workspace must not overlap on the GPU.
  */
 VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
                        int64_t loss_start, int64_t loss_end,
-                       uint32_t* ids, float* probs, int32_t* err, void* stream);
+                       uint32_t* ids, float* probs, int32_t* err,
+                       void* workspace, int64_t workspace_bytes, void* stream);
+
+
+/*
+ * Bytes of workspace with which vl_topk_rows streams ntok rows of V columns on one CTA per
+ * SM of the current device (256 CTAs when no device is present): two sets of candidate
+ * regions per CTA (about 60 KB at k = 256, 130 KB at k = 2048 for V = 128256) and 4 bytes a
+ * row; 0 when rows of that length and k do not use a workspace (rows shorter than 30720 or
+ * longer than 2^20 columns, or k above about 6% of V).
+ */
+VL_API int64_t vl_topk_workspace_bytes(int64_t ntok, int64_t V, int64_t k);
 
 /*
  * Windowed mean of per-row losses (wgpu_cross_entropy.rs: read_loss, which sums the
@@ -211,6 +256,51 @@ VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int
  */
 VL_API vl_status vl_window_mean(const float* loss, int64_t ntok, int64_t loss_start, int64_t loss_end,
                                 float* mean, void* stream);
+
+/*
+ * The frozen vocabulary head around the row losses, on chunks of rows so that the
+ * [ntok][V] logits are never held whole (cortiq-engine train_head.rs: topk, head_kl).
+ * hidden [ntok][hs] and w [V][hs] are bf16 (16-bit patterns), row-major, 16-byte
+ * aligned, hs a multiple of 8.  Per chunk, logits = hidden . w^T with bf16 inputs and
+ * fp32 accumulation and output (cuBLASLt: a plain dense GEMM), then this library's
+ * kernels.  Everything stays on the stream: no host readback between chunks.
+ * workspace: caller-owned device memory, 16-byte aligned, no initial contents needed;
+ * the call takes as many rows per chunk as it holds (at least one row:
+ * vl_*_workspace_bytes(1, ...)).  Calls that share a workspace must not overlap.
+ *
+ * vl_teacher_topk: ids/probs of the rows [loss_start, loss_end) as vl_topk_rows over the
+ *   logits (the teacher's top-k, train_head.rs topk).
+ * vl_head_kl: the student's head step (train_head.rs head_kl): per row, the CE + top-k
+ *   KL losses and gradient of vl_ce_kl_fused over the logits (window, coef, ce_coef as
+ *   there), the gradient rounded to bf16 (the page's cvt_cols), and
+ *   dx[t] = dx_scale * sum_j g[t][j] * w[j]  (the page's mm(wt, ..., 1/gscale)),
+ *   fp32 [ntok][hs], 16-byte aligned; rows outside the window get dx = 0.  ce_mean
+ *   (nullable): the windowed mean of ce_loss.  wt (nullable): the transposed weight
+ *   plane [hs][V] bf16, 16-byte aligned, as the page keeps for this GEMM; with it (and V
+ *   a multiple of 8) both GEMMs run on the tensor-core kernel of vl_gemm_bf16_tn, without
+ *   it the dx GEMM reads w through cuBLASLt.
+ */
+/*
+ * The head's GEMM on the 5th-generation tensor cores: D[M][N] = alpha * A[M][K] . B[N][K]^T,
+ * A and B bf16 (16-bit patterns), row-major, 16-byte aligned, K a multiple of 8; D fp32,
+ * row-major with stride ldd >= N.  fp32 accumulation in tensor memory (tcgen05.mma fed by
+ * TMA).  Logits are hidden . W^T; the backward dlogits . wt^T with the transposed weight
+ * plane wt (train_head.rs keeps one per slice for that GEMM).
+ */
+VL_API vl_status vl_gemm_bf16_tn(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N, int64_t K,
+                          int64_t ldd, float alpha, void* stream);
+
+VL_API int64_t vl_teacher_topk_workspace_bytes(int64_t rows, int64_t V, int64_t k);
+VL_API vl_status vl_teacher_topk(const uint16_t* hidden, int64_t hs, const uint16_t* w, int64_t V, int64_t ntok,
+                          int64_t k, int64_t loss_start, int64_t loss_end, uint32_t* ids, float* probs,
+                          int32_t* err, void* workspace, int64_t workspace_bytes, void* stream);
+VL_API int64_t vl_head_kl_workspace_bytes(int64_t rows, int64_t V);
+VL_API vl_status vl_head_kl(const uint16_t* hidden, int64_t hs, const uint16_t* w, const uint16_t* wt, int64_t V,
+                     int64_t ntok,
+                     const uint32_t* labels, const uint32_t* tid, const float* tp, int64_t k, float coef,
+                     float ce_coef, float dx_scale, int64_t loss_start, int64_t loss_end, float* dx,
+                     float* kl_loss, float* ce_loss, float* ce_mean, int32_t* err, void* workspace,
+                     int64_t workspace_bytes, void* stream);
 
 /*
  * a[i] = a[i] + b[i] for 0 <= i < n, fp32, bit-exact (train_head.rs: acc_add, which adds a

@@ -16,7 +16,7 @@ def _vl():
     return vloss
 
 
-def run_fused(x, lab, ls, le, scale, ld=None, off=0, workspace="auto"):
+def run_fused(x, lab, ls, le, scale, ld=None, off=0):
     torch = H.torch_cuda()
     vl = _vl()
     ntok, V = x.shape
@@ -29,7 +29,7 @@ def run_fused(x, lab, ls, le, scale, ld=None, off=0, workspace="auto"):
     mean = torch.full((1,), -7.0, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     vl.vl_ce_fused(view.data_ptr() if ntok else buf.data_ptr(), ld, ntok, V, labels, ls, le, scale, loss, lse,
-                   stats, mean, err, workspace)
+                   stats, mean, err)
     torch.cuda.synchronize()
     return buf, view, loss, lse, stats, mean, err
 
@@ -48,9 +48,8 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("ws", ["split", "whole_rows"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_ce_fused(name, ws):
+def test_ce_fused(name):
     if name == "tiny_workload":
         w = W.WORKLOADS["ce_tiny"]
         x, lab = W.logits(w), W.labels(w)
@@ -60,8 +59,7 @@ def test_ce_fused(name, ws):
         x = W.random_logits(ntok, V, seed=zlib.crc32(name.encode()), sigma=sigma)
         lab = W.random_labels(ntok, V, seed=zlib.crc32(name.encode()) + 1)
     ntok, V = x.shape
-    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off,
-                                                       "auto" if ws == "split" else None)
+    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
     oloss, olse, og, omean = O.ce_fused(x, lab, ls, le, scale)
     g = H.host(view)
     H.check_grad(g[:, :V], og, scale)
@@ -184,10 +182,9 @@ def test_ce_fused_beyond_on_chip_rows():
     (457, 7, 9, 1),              # rows shorter than a float4 run
     (512, 32000, 32000, 0),      # the LM workload's shape
 ])
-def test_ce_fused_tail_split(ntok, V, ld, off):
-    """The rows past the last full wave cut across all SMs: every row, its lse, loss and
-    gradient, whatever the cut points, alignment and stride; two calls in a row on the
-    same workspace (its generation advances) both match."""
+def test_ce_fused_row_counts(ntok, V, ld, off):
+    """Row counts around a wave of SMs, ragged strides and misaligned bases: every row, its
+    lse, loss and gradient; two calls in a row both match."""
     seed = ntok * 7919 + V
     x = W.random_logits(ntok, V, seed=seed, sigma=3.0)
     lab = W.random_labels(ntok, V, seed=seed + 1)
@@ -196,21 +193,21 @@ def test_ce_fused_tail_split(ntok, V, ld, off):
     for _ in range(2):
         buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
         g = H.host(view)
-        H.check_grad(g[:, :V], og, scale, "split gradient")
+        H.check_grad(g[:, :V], og, scale, "gradient")
         if ld > V:
             assert np.isnan(g[:, V:]).all()
         if off:
             assert np.isnan(H.host(buf)[:off]).all()
-        H.check_loss(H.host(loss), oloss, olse, "split loss")
-        H.check_lse(H.host(lse), olse, "split lse")
+        H.check_loss(H.host(loss), oloss, olse, "loss")
+        H.check_lse(H.host(lse), olse, "lse")
         st = H.host(stats)
         assert np.array_equal(st[:, 0], x.max(axis=1))
         H.check_mean(H.host(mean)[0], omean)
         assert int(H.host(err)[0]) == 0
 
 
-def test_ce_fused_split_bad_labels_counted_once():
-    """A bad label in a row cut over several SMs is counted once and gives a NaN loss."""
+def test_ce_fused_bad_labels_counted_once_per_row():
+    """A bad label in a row split over a cluster of CTAs is counted once and gives a NaN loss."""
     ntok, V = 40, 20000
     x = W.random_logits(ntok, V, seed=71)
     lab = W.random_labels(ntok, V, seed=72)

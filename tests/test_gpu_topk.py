@@ -9,7 +9,7 @@ from top_kl_distill_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def run_topk(x, k, ls=0, le=None, ld=None, off=0, with_err=False):
+def run_topk(x, k, ls=0, le=None, ld=None, off=0, with_err=False, workspace="auto"):
     torch = H.torch_cuda()
     from top_kl_distill_gb300 import vloss as vl
     ntok, V = x.shape
@@ -19,13 +19,15 @@ def run_topk(x, k, ls=0, le=None, ld=None, off=0, with_err=False):
     ids = torch.full((ntok, k), -1, dtype=torch.int32, device="cuda")
     probs = torch.full((ntok, k), -1.0, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    vl.vl_topk_rows(view.data_ptr(), ld, ntok, V, k, ls, le, ids, probs, err)
+    vl.vl_topk_rows(view.data_ptr(), ld, ntok, V, k, ls, le, ids, probs, err, workspace)
     torch.cuda.synchronize()
     out = H.host(ids).view(np.uint32), H.host(probs)
     return out + (int(H.host(err)[0]),) if with_err else out
 
 
 def check(x, k, ls=0, le=None, **kw):
+    """Exact against the oracle; rows of 30720 columns or more go through the streaming
+    kernel (the default workspace) and, with workspace=None, the single kernel."""
     ntok = x.shape[0]
     le = ntok if le is None else le
     ids, probs, err = run_topk(x, k, ls, le, with_err=True, **kw)
@@ -36,10 +38,29 @@ def check(x, k, ls=0, le=None, **kw):
     assert np.all(ids[~valid] == 0xFFFFFFFF) and np.all(probs[~valid] == -1.0), "rows outside the window written"
 
 
+@pytest.mark.parametrize("path", ["stream", "single_kernel"])
 @pytest.mark.parametrize("k", [256, 2048])
-def test_topk_workload_rows(k):
+def test_topk_workload_rows(k, path):
     w = W.WORKLOADS["topk"].scaled(6)
-    check(W.logits(w), k)
+    check(W.logits(w), k, workspace="auto" if path == "stream" else None)
+
+
+def test_topk_stream_few_ctas_with_fallback_rows():
+    """A workspace with candidate regions for three CTAs only: 11 rows on 3 CTAs, each
+    alternating its two region sets over four rows, with monotone rows (threshold check
+    fails, or the regions overflow) mixed in for the exact kernel."""
+    torch = H.torch_cuda()
+    from top_kl_distill_gb300 import vloss as vl
+    V, k = 40000, 300
+    x = W.random_logits(11, V, seed=51, sigma=3.0)
+    up = np.arange(V, dtype=np.float32) * np.float32(1e-3)
+    x[2], x[7] = up, up[::-1]
+    f = vl.vl_topk_workspace_bytes
+    cta = f(2, V, k) - f(1, V, k)
+    ws = torch.empty(f(11, V, k) - 8 * cta, dtype=torch.uint8, device="cuda")
+    assert cta > 0
+    check(x, k, workspace=ws)
+    check(x, k, ls=3, le=10, workspace=ws)
 
 
 @pytest.mark.parametrize("k", [1, 7, 100, 700])
@@ -55,13 +76,15 @@ def test_topk_all_equal_and_signed_zeros():
     check(x, 2048)
 
 
-def test_topk_monotone_rows():
-    """Ascending rows admit every new column (the most compactions); descending rows almost none."""
+@pytest.mark.parametrize("ws", ["auto", None])
+def test_topk_monotone_rows(ws):
+    """Ascending rows admit every new column (the most compactions, or a list overflow);
+    descending rows almost none (the threshold check fails): the exact kernel's rows."""
     V = 50000
     up = np.arange(V, dtype=np.float32)[None, :] * np.float32(1e-3)
     x = np.concatenate([up, up[:, ::-1].copy(), -up], axis=0)
     for k in (1, 256, 2048):
-        check(x, k)
+        check(x, k, workspace=ws)
 
 
 def test_topk_k_equals_v_and_misaligned():

@@ -9,6 +9,7 @@ statically, so loading the library needs no GPU).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import glob
 import os
 import shutil
 import subprocess
@@ -30,6 +31,15 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libvloss")
+
+
+def cuda_libdir() -> str:
+    """The toolkit's library directory (cuBLASLt, for the head GEMMs), next to nvcc."""
+    home = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
+    for cand in [os.path.join(home, "lib64"), *sorted(glob.glob(os.path.join(home, "targets", "*", "lib")))]:
+        if os.path.exists(os.path.join(cand, "libcublasLt.so")):
+            return cand
+    raise RuntimeError(f"libcublasLt.so not found under {home}")
 
 
 def sources() -> list[str]:
@@ -57,7 +67,9 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     with cf.ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, extra), srcs))
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    libdir = cuda_libdir()
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-L", libdir, "-lcublasLt",
+           "-Xlinker", "-rpath=" + libdir]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -1,17 +1,19 @@
 // Row engine: cross-entropy (fused, forward, backward) and top-k KL over rows of
-// fp32 vocabulary logits, one persistent CTA (or cluster of CTAs) per SM.
+// vocabulary logits, one persistent CTA (or cluster of CTAs) per SM.  The logits are
+// fp32, or bf16 (read as bf16, every sum and exponential in fp32, the gradient
+// rounded to bf16, nearest even, when it is written back).
 //
 // Layout of one launch
 //   * grid = nclusters * csize CTAs, one CTA per SM (the ring below takes
 //     ~200 KB of shared memory).  Cluster i handles rows i, i + nclusters, ...
-//   * a row slice of ncols floats is cut into a <=3-float head, a 16-byte-aligned
-//     body and a <=3-float tail.  The body is split evenly (in float4 units)
-//     across the csize CTAs of the cluster; CTA rank 0 also takes the head and
-//     the last rank the tail.
+//   * a row slice of ncols elements is cut into a head (the elements before the first
+//     16-byte boundary: at most 3 fp32 or 7 bf16), a 16-byte-aligned body and a tail
+//     of the same bound.  The body is split evenly (in 16-byte chunks) across the csize
+//     CTAs of the cluster; CTA rank 0 also takes the head and the last rank the tail.
 //   * warp 0 (one lane) is the producer: it streams each CTA's body through a
-//     ring of kSlots tiles of kTileF floats with 1-D bulk copies (TMA) signalled
+//     ring of kSlots tiles of kTileB bytes with 1-D bulk copies (TMA) signalled
 //     on per-slot mbarriers; warps 1..15 are consumers.  A consumer thread owns
-//     float4s ct, ct + NCT, ... (kVec of them) of every tile.
+//     16-byte chunks ct, ct + NCT, ... (kVec of them) of every tile.
 //
 // Modes
 //   self-contained (CE fused, KL without given statistics): the producer streams
@@ -28,17 +30,22 @@
 // Sparse columns (the label, the teacher's top-k ids).  Streaming mode gathers their
 // logits from the staged tiles as they pass and rewrites their gradient after the
 // bulk store of the row and a barrier.  Self-contained mode folds the label into
-// pass B, gathers the support logits from global memory before pass A (the row is
-// not written until after it) for the KL loss, and adds -coef * p_q at the support
-// columns with reduction adds after a barrier that follows the row's pass B.
+// pass B and gathers the support logits from global memory before pass A (the row is
+// not written until after it) for the KL loss; after a barrier that follows the row's
+// pass B it adds -coef * p_q at the support columns with reduction adds (fp32), or
+// rewrites those columns with their whole gradient from the gathered logits (bf16,
+// so that every element is rounded once).
 //
 // Sources: aprender-train wgpu_cross_entropy.rs (module doc, forward_async,
 // backward: loss = lse - s[label], gradient scale * (softmax - onehot), loss
 // window) and cortiq-engine train_head.rs (module doc and kl_rows: KL over the
-// teacher's top-k, gradient coef * (softmax - p_T)).  The pages' kernels read a
-// row three times with workgroup tree reductions; this engine reads it once.
+// teacher's top-k, gradient coef * (softmax - p_T); the f16 activations beside f32
+// logits).  The pages' kernels read a row three times with workgroup tree
+// reductions; this engine reads it once.
 #include "vl_device.cuh"
 #include "vl_internal.h"
+
+#include <cuda_bf16.h>
 
 #include <atomic>
 #include <cmath>
@@ -67,19 +74,85 @@ constexpr uint32_t kBarConsumers = 1;   // named barrier id used by consumers on
 constexpr uint32_t kPartBufs = 8;
 static_assert(2 * kPartBufs - 2 > kSlots, "partial buffers outlast the ring");
 
-static_assert(kTileF / 4 == NCT * kVec, "kVec float4s of each tile per consumer thread");
+static_assert(kTileB / 16 == NCT * kVec, "kVec 16-byte chunks of each tile per consumer thread");
 static_assert(KMAX >= 1024, "the C ABI promises k <= 1024");
 
 __device__ unsigned int g_watchdog;
 
+// ---------------------------------------------------------------- element types
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int NV = 4;        // elements per 16 bytes
+    static __device__ __forceinline__ void unpack(uint4 r, float (&f)[NV]) {
+        f[0] = __uint_as_float(r.x);
+        f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z);
+        f[3] = __uint_as_float(r.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[NV]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+    static __device__ __forceinline__ float get(const float* p) { return *p; }
+    static __device__ __forceinline__ void put(float* p, float v) { *p = v; }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int NV = 8;
+    static __device__ __forceinline__ void unpack(uint4 r, float (&f)[NV]) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);            // the element at the lower address
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    // two floats to bf16, rounded to nearest even: lo to the lower address
+    static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+        uint32_t d;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+        return d;
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[NV]) {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    }
+    static __device__ __forceinline__ float get(const __nv_bfloat16* p) {
+        return __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(p) << 16);
+    }
+    static __device__ __forceinline__ void put(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+template <typename T>
+constexpr int kTileE = kTileB / (int)sizeof(T);    // elements per tile
+
+__device__ __forceinline__ uint4 ld_shared_u4(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+    return v;
+}
+
+__device__ __forceinline__ void st_global_u4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_global_u4_hint(void* p, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy) : "memory");
+}
+
+// ---------------------------------------------------------------- shared memory
+
 struct alignas(128) Smem {
-    float ring[kSlots][kTileF];
+    alignas(16) unsigned char ring[kSlots][kTileB];
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
-    uint64_t xbar[4];                   // cluster exchange of (max, sum)
-    uint64_t lbar[2];                   // cluster exchange of KL loss parts (rank 0)
+    uint64_t xbar[4];                   // cluster exchange of (max, sum, KL a, KL b)
     float4 xbuf[4][kMaxCluster];        // (max, sum, KL a, KL b) of each rank's part
-    float lbuf[2][kMaxCluster];
     float4 wred[2][NCW];                // per warp: (max, sum, KL a, KL b)
     uint64_t abar[kPartBufs];           // self-contained CE: every warp's pass A partial is in
     float2 wpart[kPartBufs][NCW];
@@ -91,8 +164,10 @@ struct alignas(128) Smem {
             float ks[2][KMAX];               // the logit at that column, gathered as its tile passes
         };
         struct {                        // self-contained mode: support of the last kSupBufs rows
-            int ecol[kSupBufs][KSELF];       // support column (slice-relative; -1 elsewhere)
+            alignas(16) int ecol[kSupBufs][KSELF];   // support column (slice-relative; -1 elsewhere)
             float ep[kSupBufs][KSELF];
+            unsigned short es[kSupBufs][KSELF];      // bf16: the gathered logit (exact), for the rewrite
+            float erow[kSupBufs][3];                 // bf16: m, lnS and the label column of the row
         };
     };
     int abort;
@@ -103,23 +178,25 @@ static_assert(sizeof(Smem) <= 227 * 1024, "shared memory of one CTA");
 
 // Columns of one row slice handled by CTA `rank` of `c` (relative to the slice start).
 struct Part {
-    int h;     // head length (first columns up to the 16-byte boundary)
+    int h;     // head length (elements before the first 16-byte boundary)
     int hn;    // head columns this CTA handles
     int b0;    // first body column of this CTA
-    int bn;    // body columns of this CTA (a multiple of 4)
+    int bn;    // body columns of this CTA (a multiple of a 16-byte chunk)
     int t0;    // first tail column
     int tn;    // tail columns this CTA handles
     int lo;    // this CTA owns columns [lo, hi)
     int hi;
 };
 
-__device__ __forceinline__ Part part_of(const float* rowp, int n, int rank, int c) {
+template <typename T>
+__device__ __forceinline__ Part part_of(const T* rowp, int n, int rank, int c) {
+    constexpr int NV = Elem<T>::NV;
     Part p;
-    const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
-    int h = (4 - mis) & 3;
+    const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) & 15u) / sizeof(T));
+    int h = (NV - mis) & (NV - 1);
     if (h > n) h = n;
-    const int bt = (n - h) & ~3;
-    const int per = (((bt >> 2) + c - 1) / c) * 4;
+    const int bt = (n - h) & ~(NV - 1);
+    const int per = ((bt / NV + c - 1) / c) * NV;
     const int s = min(rank * per, bt);
     const int e = min((rank + 1) * per, bt);
     p.h = h;
@@ -133,107 +210,18 @@ __device__ __forceinline__ Part part_of(const float* rowp, int n, int rank, int 
     return p;
 }
 
-// Columns of units [u0, u1) of a row slice of n floats, cut into U = ceil(n / 4) units:
-// unit u is body float4 min(u, nb4) (nb4 body float4s after the head); the head goes
-// with the part that starts at unit 0, the tail with the part that ends at unit U.
-// The parts of any partition of [0, U) cover the row exactly once.
-__device__ __forceinline__ Part part_units(const float* rowp, int n, int U, int u0, int u1) {
-    Part p;
-    const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
-    int h = (4 - mis) & 3;
-    if (h > n) h = n;
-    const int nb4 = (n - h) >> 2;
-    const int f0 = min(u0, nb4), f1 = min(u1, nb4);
-    p.h = h;
-    p.hn = u0 == 0 ? h : 0;
-    p.b0 = h + 4 * f0;
-    p.bn = 4 * (f1 - f0);
-    p.t0 = h + 4 * nb4;
-    p.tn = u1 == U ? n - p.t0 : 0;
-    p.lo = u0 == 0 ? 0 : p.b0;
-    p.hi = u1 == U ? n : p.b0 + p.bn;
-    return p;
+// The head and tail columns: thread ct < hn takes head column ct, thread NV + i the
+// tail column t0 + i.
+template <typename T>
+__device__ __forceinline__ bool has_ht(const Part& pt, int ct) {
+    constexpr int NV = Elem<T>::NV;
+    return ct < pt.hn || (ct >= NV && ct - NV < pt.tn);
 }
 
-// ---------------------------------------------------------------- tail split
-//
-// With G CTAs and R rows, every CTA first takes q = R / G whole rows (b, b + G, ...).
-// The T = R - qG rows left over are not given whole to T of the CTAs (which would leave
-// the others idle for a row's time): their units, T * U in all, are cut into G equal
-// ranges, CTA b taking units [b TU / G, (b + 1) TU / G).  A range is shorter than a
-// row, so it touches at most two rows: the CTA's tail segments 0 and 1.  A segment's
-// (max, sum) is published in the workspace; before a segment's pass B its CTA merges
-// the parts of the row from every CTA that holds one, in CTA order, so that all of
-// them use bit-identical row statistics.
-//
-// Workspace words: [0] generation, [1] ticket, then slot (b, s) at word
-// 4 + 4 (2b + s) = {max, sum, sequence, -}.  A launch reads the generation g at its
-// start and marks its slots with sequence g + 1; the last CTA to finish (ticket)
-// advances the generation, so a launch never reads a slot left by an earlier one.
-
-struct Item {
-    long long r;     // row
-    int u0, u1;      // units [u0, u1) of the row
-    int which;       // -1: a whole row; 0 / 1: this CTA's first / second tail segment
-    long long j;     // tail row index (which >= 0)
-};
-
-__device__ __forceinline__ bool item_at(const RowParams& P, long long i, int U, Item& it) {
-    const long long G = gridDim.x, b = blockIdx.x;
-    const long long q = P.ntok / G;
-    if (i < q) {
-        it.r = b + i * G;
-        it.u0 = 0;
-        it.u1 = U;
-        it.which = -1;
-        it.j = -1;
-        return true;
-    }
-    const long long TU = (P.ntok - q * G) * (long long)U;
-    const long long lo = b * TU / G, hi = (b + 1) * TU / G;
-    if (lo >= hi) return false;
-    const long long j0 = lo / U, j1 = (hi - 1) / U;
-    if (i == q) {
-        it.j = j0;
-        it.u0 = (int)(lo - j0 * U);
-        it.u1 = (int)(min(hi, (j0 + 1) * U) - j0 * U);
-    } else if (i == q + 1 && j1 > j0) {
-        it.j = j1;
-        it.u0 = 0;
-        it.u1 = (int)(hi - j1 * U);
-    } else {
-        return false;
-    }
-    it.which = (int)(i - q);
-    it.r = q * G + it.j;
-    return true;
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned int* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned int* ws_slot(const RowParams& P, long long b, int which) {
-    return P.ws + kWsHeaderWords + 4 * (2 * b + which);
-}
-
-// This CTA's (max, sum) of tail segment `which`, for the other parts of its row.
-__device__ __forceinline__ void publish_part(const RowParams& P, int which, MaxSum ms, uint32_t epoch) {
-    unsigned int* sl = ws_slot(P, blockIdx.x, which);
-    asm volatile("st.global.cg.v2.f32 [%0], {%1, %2};" :: "l"(sl), "f"(ms.m), "f"(ms.s) : "memory");
-    st_release_u32(sl + 2, epoch);
+template <typename T>
+__device__ __forceinline__ int ht_col(const Part& pt, int ct) {
+    constexpr int NV = Elem<T>::NV;
+    return ct < pt.hn ? ct : pt.t0 + ct - NV;
 }
 
 template <int OP>
@@ -242,50 +230,70 @@ __device__ __forceinline__ bool row_loaded(const RowParams& P, long long r) {
     return r >= P.ls && r < P.le;
 }
 
+template <typename T>
+__device__ __forceinline__ T* row_ptr(const RowParams& P, long long r) {
+    return static_cast<T*>(P.x) + r * P.ld + P.col0;
+}
+
 // softmax value from the row statistics: exp((s - m) - lnS)
 __device__ __forceinline__ float soft(float s, float m, float lnS) {
     return ex2(((s - m) - lnS) * kLog2e);
 }
 
-__device__ __forceinline__ void sub_at(float4& o, unsigned d, float a) {
-    if (d == 0) o.x -= a;
-    else if (d == 1) o.y -= a;
-    else if (d == 2) o.z -= a;
-    else o.w -= a;
-}
-
-// (max, sum) update with kVec float4s (absent values are -inf): one max update,
-// independent exponentials summed as a tree.
-__device__ __forceinline__ void ms_addv(MaxSum& a, const float4 (&v)[kVec]) {
-    float mx = fmaxf(fmaxf(v[0].x, v[0].y), fmaxf(v[0].z, v[0].w));
+// (max, sum) update with kVec chunks of NV values (absent values are -inf): one max
+// update, independent exponentials summed as a tree.
+template <int NV>
+__device__ __forceinline__ void ms_addv(MaxSum& a, const float (&v)[kVec][NV]) {
+    float mx = v[0][0];
 #pragma unroll
-    for (int u = 1; u < kVec; ++u) mx = fmaxf(mx, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+    for (int u = 0; u < kVec; ++u)
+#pragma unroll
+        for (int i = 0; i < NV; ++i) mx = fmaxf(mx, v[u][i]);
     if (mx > a.m) {
         a.s *= ex2((a.m - mx) * kLog2e);
         a.m = mx;
     }
     float e[kVec];
 #pragma unroll
-    for (int u = 0; u < kVec; ++u)
-        e[u] = (ex2((v[u].x - a.m) * kLog2e) + ex2((v[u].y - a.m) * kLog2e)) +
-               (ex2((v[u].z - a.m) * kLog2e) + ex2((v[u].w - a.m) * kLog2e));
+    for (int u = 0; u < kVec; ++u) {
+        float q[NV / 2];
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i)
+            q[i] = ex2((v[u][2 * i] - a.m) * kLog2e) + ex2((v[u][2 * i + 1] - a.m) * kLog2e);
+#pragma unroll
+        for (int w = NV / 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) q[i] += q[i + w];
+        e[u] = q[0];
+    }
     float t = e[0];
 #pragma unroll
     for (int u = 1; u < kVec; ++u) t += e[u];
     a.s += t;
 }
 
+// Chunk j of tile `slot` into v (absent chunks: -inf).
+template <typename T>
+__device__ __forceinline__ void load_chunk(const Smem& S, uint32_t slot, int j, int n16, float (&v)[Elem<T>::NV]) {
+    if (j < n16) {
+        Elem<T>::unpack(ld_shared_u4(&S.ring[slot][16 * j]), v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < Elem<T>::NV; ++i) v[i] = -INFINITY;
+    }
+}
+
 // ---------------------------------------------------------------- producer
 
 // Issue the body tiles of one row part; false if a wait gave up.
-__device__ __forceinline__ bool issue_body(const RowParams& P, Smem& S, const float* rowp, const Part& pt,
-                                           uint32_t& g) {
-    for (int c0 = 0; c0 < pt.bn; c0 += kTileF) {
+template <typename T>
+__device__ __forceinline__ bool issue_body(const RowParams& P, Smem& S, const T* rowp, const Part& pt, uint32_t& g) {
+    for (int c0 = 0; c0 < pt.bn; c0 += kTileE<T>) {
         // test hook: CTA 0 stops before this tile, so the consumers' wait for it runs out
         if ((long long)g == P.withhold && blockIdx.x == 0) return false;
         const uint32_t slot = g % kSlots, use = g / kSlots;
         if (use > 0 && !wait_parity<false>(&S.empty[slot], (use - 1) & 1u, &S.abort, &g_watchdog, P.wait_limit)) return false;
-        const uint32_t bytes = (uint32_t)min(kTileF, pt.bn - c0) * 4u;
+        const uint32_t bytes = (uint32_t)min(kTileE<T>, pt.bn - c0) * (uint32_t)sizeof(T);
         mbar_arrive_expect_tx(&S.full[slot], bytes);
         bulk_g2s(S.ring[slot], rowp + pt.b0 + c0, bytes, &S.full[slot]);
         ++g;
@@ -293,48 +301,28 @@ __device__ __forceinline__ bool issue_body(const RowParams& P, Smem& S, const fl
     return true;
 }
 
+template <typename T>
 __device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long long r, int rank, uint32_t& g) {
-    const float* rowp = P.x + r * P.ld + P.col0;
-    return issue_body(P, S, rowp, part_of(rowp, (int)P.ncols, rank, P.csize), g);
-}
-
-__device__ __forceinline__ bool issue_item(const RowParams& P, Smem& S, const Item& it, int U, uint32_t& g) {
-    const float* rowp = P.x + it.r * P.ld + P.col0;
-    return issue_body(P, S, rowp, part_units(rowp, (int)P.ncols, U, it.u0, it.u1), g);
-}
-
-// Tail split: the items (whole rows, then tail segments) in the two-pass order.
-__device__ void producer_split(const RowParams& P, Smem& S) {
-    const int U = (int)((P.ncols + 3) >> 2);
-    uint32_t g = 0;
-    Item it, prev;
-    bool have_prev = false, ok = true;
-    for (long long i = 0; ok && item_at(P, i, U, it); ++i) {
-        ok = issue_item(P, S, it, U, g);
-        if (ok && have_prev) ok = issue_item(P, S, prev, U, g);
-        prev = it;
-        have_prev = true;
-    }
-    if (ok && have_prev && !S.abort) issue_item(P, S, prev, U, g);
-    S.issued = g;
+    const T* rowp = row_ptr<T>(P, r);
+    return issue_body<T>(P, S, rowp, part_of<T>(rowp, (int)P.ncols, rank, P.csize), g);
 }
 
 // Tile order: one pass per row for the streaming and reduce modes; for the
 // self-contained mode pass A of a row, then pass B of the row before it, so the
 // reads of the next row are in flight while the current one is written.
-template <int OP, bool RES>
+template <typename T, int OP, bool RES>
 __device__ void producer(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     uint32_t g = 0;
     long long prev = -1;
     for (long long r = cid; r < P.ntok; r += ncl) {
         if (!row_loaded<OP>(P, r)) continue;
-        if (!issue_part(P, S, r, rank, g)) break;
+        if (!issue_part<T>(P, S, r, rank, g)) break;
         if (RES) {
-            if (prev >= 0 && !issue_part(P, S, prev, rank, g)) break;
+            if (prev >= 0 && !issue_part<T>(P, S, prev, rank, g)) break;
             prev = r;
         }
     }
-    if (RES && prev >= 0 && !S.abort) issue_part(P, S, prev, rank, g);
+    if (RES && prev >= 0 && !S.abort) issue_part<T>(P, S, prev, rank, g);
     S.issued = g;
 }
 
@@ -347,39 +335,43 @@ __device__ void drain(Smem& S, long long limit) {
 
 // ---------------------------------------------------------------- consumer helpers
 
-__device__ void zero_part(float* rowp, const Part& pt, int ct) {
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = ct; i < (pt.bn >> 2); i += NCT) st_global_v4(rowp + pt.b0 + 4 * i, z);
-    if (ct < pt.hn) rowp[ct] = 0.f;
-    if (ct >= 4 && ct - 4 < pt.tn) rowp[pt.t0 + ct - 4] = 0.f;
+template <typename T>
+__device__ void zero_part(T* rowp, const Part& pt, int ct) {
+    constexpr int NV = Elem<T>::NV;
+    for (int i = ct; i < pt.bn / NV; i += NCT) st_global_u4(rowp + pt.b0 + NV * i, make_uint4(0u, 0u, 0u, 0u));
+    if (has_ht<T>(pt, ct)) Elem<T>::put(rowp + ht_col<T>(pt, ct), 0.f);
 }
 
 // A sparse column this thread looks after: where it sits in the row part, and its
 // logit once the tile holding it has passed.
 struct Sparse {
     int col;     // slice-relative column, -1 if none
-    int rel;     // column - b0 inside this CTA's body (tile = rel / kTileF), -1 for head/tail
+    int rel;     // column - b0 inside this CTA's body (tile = rel / tile elements), -1 for head/tail
     float s;     // the logit
 };
 
-__device__ __forceinline__ void locate(Sparse& e, const Part& pt, const float* rowp) {
+template <typename T>
+__device__ __forceinline__ void locate(Sparse& e, const Part& pt, const T* rowp) {
     if (e.col >= pt.b0 && e.col < pt.b0 + pt.bn) {
         e.rel = e.col - pt.b0;
     } else {
         e.rel = -1;
-        e.s = rowp[e.col];     // head or tail: read before anything of the row is written
+        e.s = Elem<T>::get(rowp + e.col);     // head or tail: read before anything of the row is written
     }
 }
 
-__device__ __forceinline__ void gather(Sparse& e, int t, const float* tile) {
-    if (e.rel >= 0 && (e.rel / kTileF) == t) e.s = tile[e.rel % kTileF];
+template <typename T>
+__device__ __forceinline__ void gather(Sparse& e, int t, const unsigned char* tile) {
+    if (e.rel >= 0 && (e.rel / kTileE<T>) == t) e.s = Elem<T>::get(reinterpret_cast<const T*>(tile) + e.rel % kTileE<T>);
 }
 
+template <typename T>
 __device__ __forceinline__ void gather_support(Smem& S, uint32_t kb, const int (&erel)[EPT], int ct, int t,
-                                               const float* tile) {
+                                               const unsigned char* tile) {
 #pragma unroll
     for (int i = 0; i < EPT; ++i)
-        if (erel[i] >= 0 && erel[i] / kTileF == t) S.ks[kb][ct + i * NCT] = tile[erel[i] % kTileF];
+        if (erel[i] >= 0 && erel[i] / kTileE<T> == t)
+            S.ks[kb][ct + i * NCT] = Elem<T>::get(reinterpret_cast<const T*>(tile) + erel[i] % kTileE<T>);
 }
 
 // (max, sum) of n partials: the max first, then the sums rescaled independently.
@@ -412,16 +404,31 @@ __device__ __forceinline__ Part4 combine4(const float4* part, int n) {
     return Part4{MaxSum{M, T}, A, B};
 }
 
-// ---------------------------------------------------------------- consumer
+// The gradient of a chunk: c1 * exp(x - m - lnS) per element, as 2^(x log2 e - m log2 e - K)
+// with K = lnS log2 e - log2 c1 when c1 >= 0 (the scale folded into the exponent).
+template <int NV>
+__device__ __forceinline__ void grad_chunk(const float (&x)[NV], float (&o)[NV], bool fold, float m, float lnS, float K,
+                                           float c1) {
+    if (fold) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) o[i] = ex2(fmaf(x[i] - m, kLog2e, -K));
+    } else {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) o[i] = c1 * soft(x[i], m, lnS);
+    }
+}
 
-template <int OP, bool RES>
+// ---------------------------------------------------------------- streaming consumer
+
+template <typename T, int OP>
 __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     constexpr bool kKL = OP == kKl;
+    constexpr int NV = Elem<T>::NV;
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
     const int c = P.csize;
     const int ncols = (int)P.ncols;
-    uint32_t g = 0, nred = 0, nloss = 0, nlx = 0, nrow = 0;
+    uint32_t g = 0, nred = 0, nloss = 0, nrow = 0;
     const bool has_label = (OP != kKl) || (P.labels != nullptr && P.ce_coef != 0.f);
     const float cg = P.cg;
     // the label and support entry q = ct of the next row, loaded one row ahead
@@ -438,12 +445,12 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
         const uint32_t lab_r = nlab, id0 = nid;
         const float p0 = np;
         prefetch(r + ncl);
-        float* rowp = P.x + r * P.ld + P.col0;
-        const Part pt = part_of(rowp, ncols, rank, c);
+        T* rowp = row_ptr<T>(P, r);
+        const Part pt = part_of<T>(rowp, ncols, rank, c);
         const bool inwin = r >= P.ls && r < P.le;
-        const int nt = (pt.bn + kTileF - 1) / kTileF;
+        const int nt = (pt.bn + kTileE<T> - 1) / kTileE<T>;
         if (!row_loaded<OP>(P, r)) {
-            zero_part(rowp, pt, ct);
+            zero_part<T>(rowp, pt, ct);
             if (ct == 0 && rank == 0 && P.loss) P.loss[r] = 0.f;
             continue;
         }
@@ -461,7 +468,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
         }
         if (bad_label && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
         Sparse lab{-1, -1, 0.f};
-        if (ct == LT && jl >= pt.lo && jl < pt.hi) { lab.col = jl; locate(lab, pt, rowp); }
+        if (ct == LT && jl >= pt.lo && jl < pt.hi) { lab.col = jl; locate<T>(lab, pt, rowp); }
         // support entry q = ct + i * NCT: its body offset in erel[i] (-1: head/tail or none)
         int erel[EPT] = {-1, -1, -1};
         if (kKL && inwin) {
@@ -481,35 +488,33 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                     S.kp[kb][q] = i == 0 ? p0 : P.tp[r * P.k + q];
                     if (col >= 0) {
                         if (col >= pt.b0 && col < pt.b0 + pt.bn) erel[i] = col - pt.b0;
-                        else S.ks[kb][q] = rowp[col];    // head or tail: before anything is written
+                        else S.ks[kb][q] = Elem<T>::get(rowp + col);    // head or tail: before anything is written
                     }
                 }
             }
         }
 
         // head and tail columns: one per thread, finished after the sparse barrier
-        const bool has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
-        const int jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
-        const float ht = has_ht ? rowp[jht] : 0.f;
+        const bool hht = has_ht<T>(pt, ct);
+        const int jht = ht_col<T>(pt, ct);
+        const float ht = hht ? Elem<T>::get(rowp + jht) : 0.f;
         float m, lnS;
 
-        if (OP == kCeFwd || RES) {
-            // ---- pass A: (max, sum) online over the streamed tiles; sparse logits gathered
+        if (OP == kCeFwd) {
+            // ---- pass A: (max, sum) online over the streamed tiles; the label's logit gathered
             MaxSum ms = ms_empty();
-            if (has_ht) ms_add(ms, ht);
+            if (hht) ms_add(ms, ht);
             for (int t = 0; t < nt; ++t) {
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
                 wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-                const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+                const int n16 = min(kTileE<T>, pt.bn - t * kTileE<T>) / NV;
+                float v[kVec][NV];
 #pragma unroll
-                for (int u = 0; u < kVec; ++u) {
-                    const int j = u * NCT + ct;
-                    if (j < n4) ms_add4(ms, ld_shared_v4(&S.ring[slot][j * 4]));
-                }
-                if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
-                if (ct == LT) gather(lab, t, S.ring[slot]);
+                for (int u = 0; u < kVec; ++u) load_chunk<T>(S, slot, u * NCT + ct, n16, v[u]);
+                if (ct == LT) gather<T>(lab, t, S.ring[slot]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
+                ms_addv<NV>(ms, v);
             }
             g += (uint32_t)nt;
             ms = ms_warp_reduce(ms);
@@ -524,50 +529,38 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 if (P.lse_out) P.lse_out[r] = m + lnS;
                 if (P.stats_out) { P.stats_out[2 * r] = m; P.stats_out[2 * r + 1] = lnS; }
             }
-            if (OP == kCeFwd) {
-                if (ct == LT) {
-                    if (!inwin) P.loss[r] = 0.f;
-                    else if (bad_label) P.loss[r] = __int_as_float(0x7fc00000);
-                    else if (lab.col >= 0) P.loss[r] = (m - lab.s) + lnS;
-                }
-                continue;
+            if (ct == LT) {
+                if (!inwin) P.loss[r] = 0.f;
+                else if (bad_label) P.loss[r] = __int_as_float(0x7fc00000);
+                else if (lab.col >= 0) P.loss[r] = (m - lab.s) + lnS;
             }
-        } else {
-            if (P.stats_in) { m = P.stats_in[2 * r]; lnS = P.stats_in[2 * r + 1]; }
-            else { m = P.lse_in[r]; lnS = 0.f; }
+            continue;
         }
+        if (P.stats_in) { m = P.stats_in[2 * r]; lnS = P.stats_in[2 * r + 1]; }
+        else { m = P.lse_in[r]; lnS = 0.f; }
 
         // ---- pass B: each tile turned into gradient as it lands (zeros outside the window)
         {
             const float c1 = inwin ? cg : 0.f;
-            // c1 * exp(d - lnS) = 2^(d * log2e - K), K = lnS * log2e - log2(c1), for c1 >= 0
             const bool fold = c1 >= 0.f;
             const float K = fold ? lnS * kLog2e - log2f(c1) : 0.f;
             const uint64_t pol = l2_evict_first();
             for (int t = 0; t < nt; ++t) {
                 const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
                 wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-                const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
+                const int n16 = min(kTileE<T>, pt.bn - t * kTileE<T>) / NV;
 #pragma unroll
                 for (int u = 0; u < kVec; ++u) {
                     const int j = u * NCT + ct;
-                    if (j < n4) {
-                        const float4 x = ld_shared_v4(&S.ring[slot][j * 4]);
-                        float4 o;
-                        if (fold) {
-                            o = make_float4(ex2(fmaf(x.x - m, kLog2e, -K)), ex2(fmaf(x.y - m, kLog2e, -K)),
-                                            ex2(fmaf(x.z - m, kLog2e, -K)), ex2(fmaf(x.w - m, kLog2e, -K)));
-                        } else {
-                            o = make_float4(c1 * soft(x.x, m, lnS), c1 * soft(x.y, m, lnS),
-                                            c1 * soft(x.z, m, lnS), c1 * soft(x.w, m, lnS));
-                        }
-                        st_global_v4_hint(rowp + pt.b0 + t * kTileF + 4 * j, o, pol);
+                    if (j < n16) {
+                        float x[NV], o[NV];
+                        Elem<T>::unpack(ld_shared_u4(&S.ring[slot][16 * j]), x);
+                        grad_chunk<NV>(x, o, fold, m, lnS, K, c1);
+                        st_global_u4_hint(rowp + pt.b0 + t * kTileE<T> + NV * j, Elem<T>::pack(o), pol);
                     }
                 }
-                if (!RES) {
-                    if (kKL) gather_support(S, kb, erel, ct, t, S.ring[slot]);
-                    if (ct == LT) gather(lab, t, S.ring[slot]);
-                }
+                if (kKL) gather_support<T>(S, kb, erel, ct, t, S.ring[slot]);
+                if (ct == LT) gather<T>(lab, t, S.ring[slot]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
             }
@@ -578,7 +571,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
         //      the support ids, and the head/tail columns with their corrections
         named_sync(kBarConsumers, NCT);
         float lacc = 0.f;
-        if (has_ht) {
+        if (hht) {
             float o = 0.f;
             if (inwin) {
                 o = cg * soft(ht, m, lnS);
@@ -587,7 +580,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                         if (S.kcol[kb][j] == jht) o -= P.coef * S.kp[kb][j];
                 if (jht == jl) o -= P.ce_coef;
             }
-            rowp[jht] = o;
+            Elem<T>::put(rowp + jht, o);
         }
         if (inwin) {
             if (kKL) {
@@ -615,7 +608,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                     if (first) {
                         float o = cg * soft(sq, m, lnS) - P.coef * psum;
                         if (col == jl) o -= P.ce_coef;
-                        rowp[col] = o;
+                        Elem<T>::put(rowp + col, o);
                     }
                 }
             }
@@ -623,12 +616,12 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 bool in_support = false;
                 if (kKL)
                     for (int j = 0; j < P.k; ++j) in_support |= S.kcol[kb][j] == lab.col;
-                if (!in_support) rowp[lab.col] = cg * soft(lab.s, m, lnS) - P.ce_coef;
+                if (!in_support) Elem<T>::put(rowp + lab.col, cg * soft(lab.s, m, lnS) - P.ce_coef);
             }
         }
 
-        // ---- losses
-        if (OP == kCeFused || OP == kCeBwd) {
+        // ---- losses (streaming launches run one CTA per row: c == 1)
+        if (OP == kCeBwd) {
             if (P.loss) {
                 if (ct == LT && inwin && lab.col >= 0) P.loss[r] = (m - lab.s) + lnS;
                 if (rank == 0 && ct == LT) {
@@ -646,20 +639,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
             if (ct == 0) {
                 float L = 0.f;
                 for (int w = 0; w < NCW; ++w) L += S.wloss[b][w];
-                if (c == 1) {
-                    P.loss[r] = L;
-                } else {
-                    const uint32_t lb = nlx & 1u, lpar = (nlx >> 1) & 1u;
-                    ++nlx;
-                    if (rank == 0) mbar_arrive_expect_tx(&S.lbar[lb], 4u * (uint32_t)c);
-                    st_async_f32(map_to_rank(&S.lbuf[lb][rank], 0u), L, map_to_rank(&S.lbar[lb], 0u));
-                    if (rank == 0) {
-                        wait_parity<true>(&S.lbar[lb], lpar, &S.abort, &g_watchdog, P.wait_limit);
-                        float T = 0.f;
-                        for (int q = 0; q < c; ++q) T += S.lbuf[lb][q];
-                        P.loss[r] = T;
-                    }
-                }
+                P.loss[r] = L;
             }
         }
     }
@@ -670,7 +650,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
 // A row whose pass A is done and whose pass B is still to come.
 struct Pending {
     long long r;
-    float* rowp;
+    void* rowp;
     Part pt;
     int nt;
     bool inwin, bad;
@@ -682,18 +662,17 @@ struct Pending {
     uint32_t xb, xpar;   // cluster exchange buffer of its statistics and the phase to wait for
     uint32_t ab, apar;   // CE: buffer of the warps' pass A partials and the phase to wait for
     bool first;          // this part holds column 0 of the row: it writes lse, stats, out-of-window loss
-    int which;           // tail split: -1 whole row, else the tail segment
-    long long j;         // tail split: tail row index
 };
 
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
 // label's one-hot folded in.  The teacher support is left to scatter_support.
-template <int OP>
+template <typename T, int OP>
 __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane) {
+    constexpr int NV = Elem<T>::NV;
+    T* const rowp = static_cast<T*>(w.rowp);
     // the CE loss: the fused CE output, or beside the KL when labels come with it
     float* const ce_out = OP == kCeFused ? P.loss : OP == kKl ? P.ce_loss : nullptr;
     const float c1 = w.inwin ? P.cg : 0.f;
-    // c1 * exp(d - lnS) = 2^(d * log2e - K) with K = lnS * log2e - log2(c1), for c1 >= 0
     const bool fold = c1 >= 0.f;
     // the gradient lines are done with: written back first, ahead of the logits that
     // pass B of the next row still re-reads from L2
@@ -702,38 +681,35 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     for (int t = 0; t < w.nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-        const int n4 = min(kTileF, w.pt.bn - t * kTileF) >> 2;
-        float4 v[kVec];
+        const int n16 = min(kTileE<T>, w.pt.bn - t * kTileE<T>) / NV;
+        uint4 raw[kVec];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int j = u * NCT + ct;
-            if (j < n4) v[u] = ld_shared_v4(&S.ring[slot][j * 4]);
+            if (j < n16) raw[u] = ld_shared_u4(&S.ring[slot][16 * j]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int j = u * NCT + ct;
-            if (j < n4) {
-                const int c0 = w.pt.b0 + t * kTileF + 4 * j;
-                const float4 x = v[u];
-                float4 o;
-                if (fold) {
-                    o = make_float4(ex2(fmaf(x.x - w.m, kLog2e, -K)), ex2(fmaf(x.y - w.m, kLog2e, -K)),
-                                    ex2(fmaf(x.z - w.m, kLog2e, -K)), ex2(fmaf(x.w - w.m, kLog2e, -K)));
-                } else {
-                    o = make_float4(c1 * soft(x.x, w.m, w.lnS), c1 * soft(x.y, w.m, w.lnS),
-                                    c1 * soft(x.z, w.m, w.lnS), c1 * soft(x.w, w.m, w.lnS));
-                }
+            if (j < n16) {
+                const int c0 = w.pt.b0 + t * kTileE<T> + NV * j;
+                float x[NV], o[NV];
+                Elem<T>::unpack(raw[u], x);
+                grad_chunk<NV>(x, o, fold, w.m, w.lnS, K, c1);
                 if (w.inwin) {
                     const unsigned d = (unsigned)(w.jl - c0);
-                    if (d < 4u) {
-                        const float xs = d == 0 ? x.x : d == 1 ? x.y : d == 2 ? x.z : x.w;
-                        sub_at(o, d, P.ce_coef);
-                        if (ce_out) ce_out[w.r] = (w.m - xs) + w.lnS;
+                    if (d < (unsigned)NV) {
+#pragma unroll
+                        for (int i = 0; i < NV; ++i)
+                            if ((unsigned)i == d) {
+                                o[i] -= P.ce_coef;
+                                if (ce_out) ce_out[w.r] = (w.m - x[i]) + w.lnS;
+                            }
                     }
                 }
-                st_global_v4_hint(w.rowp + c0, o, pol);
+                st_global_u4_hint(rowp + c0, Elem<T>::pack(o), pol);
             }
         }
     }
@@ -744,7 +720,7 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
             o -= P.ce_coef;
             if (ce_out) ce_out[w.r] = (w.m - w.ht) + w.lnS;
         }
-        w.rowp[w.jht] = o;
+        Elem<T>::put(rowp + w.jht, o);
     }
     if (ce_out && w.first && ct == LT) {
         if (!w.inwin) ce_out[w.r] = 0.f;
@@ -779,29 +755,55 @@ __device__ __forceinline__ void settle(const RowParams& P, Smem& S, Pending& w, 
     }
 }
 
-// -coef * p_q added at every support column of loaded row r (buffer sb).  Reduction
-// adds, so repeated ids sum.  Runs after a barrier that follows the row's pass B:
-// the barrier orders every thread's gradient store before these adds.
+// The teacher's part of the gradient at every support column of loaded row r (buffer
+// sb).  Runs after a barrier that follows the row's pass B, which orders every
+// thread's gradient store before it.  fp32: -coef * p_q added with reduction adds, so
+// repeated ids sum.  bf16: the column's whole gradient, cg * p_S - coef * (sum of its
+// entries' p) - ce_coef * [label], computed from the gathered logit and written once
+// (by the column's lowest entry), so that it is rounded to bf16 once.
+template <typename T>
 __device__ __forceinline__ void scatter_support(const RowParams& P, const Smem& S, long long r, uint32_t sb, int ct) {
-    float* rowp = P.x + r * P.ld + P.col0;
-    for (int q = ct; q < P.k; q += NCT) {
-        const int col = S.ecol[sb][q];
-        if (col >= 0) atomicAdd(rowp + col, -P.coef * S.ep[sb][q]);
+    T* rowp = row_ptr<T>(P, r);
+    if constexpr (sizeof(T) == 4) {
+        for (int q = ct; q < P.k; q += NCT) {
+            const int col = S.ecol[sb][q];
+            if (col >= 0) atomicAdd(reinterpret_cast<float*>(rowp) + col, -P.coef * S.ep[sb][q]);
+        }
+    } else {
+        const float m = S.erow[sb][0], lnS = S.erow[sb][1];
+        const int jl = __float_as_int(S.erow[sb][2]);
+        for (int q = ct; q < P.k; q += NCT) {
+            const int col = S.ecol[sb][q];
+            if (col < 0) continue;
+            bool first = true;
+            float psum = 0.f;
+            for (int j = 0; j < P.k; ++j)
+                if (S.ecol[sb][j] == col) {
+                    first &= j >= q;
+                    psum += S.ep[sb][j];
+                }
+            if (!first) continue;
+            const float s = __uint_as_float((uint32_t)S.es[sb][q] << 16);
+            float o = P.cg * soft(s, m, lnS) - P.coef * psum;
+            if (col == jl) o -= P.ce_coef;
+            Elem<T>::put(rowp + col, o);
+        }
     }
 }
 
-template <int OP>
+template <typename T, int OP>
 __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     constexpr bool kKL = OP == kKl;
+    constexpr int NV = Elem<T>::NV;
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
     const int c = P.csize;
     const int ncols = (int)P.ncols;
     const bool has_label = (OP != kKl) || P.labels != nullptr;
     // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
-    const bool nobar = !kKL && c == 1 && ncols >= 8;
+    const bool nobar = !kKL && c == 1 && ncols >= 2 * NV;
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
-    long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (loss, support scatter owed)
+    long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (support scatter owed)
     uint32_t nlab = 0, nid = 0;
     float np = 0.f;
     auto prefetch = [&](long long rr) {
@@ -817,11 +819,11 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         const uint32_t lab_r = nlab, id0 = nid;
         const float p0 = np;
         prefetch(r + ncl);
-        float* rowp = P.x + r * P.ld + P.col0;
-        const Part pt = part_of(rowp, ncols, rank, c);
+        T* rowp = row_ptr<T>(P, r);
+        const Part pt = part_of<T>(rowp, ncols, rank, c);
         const bool inwin = r >= P.ls && r < P.le;
         if (!row_loaded<OP>(P, r)) {
-            zero_part(rowp, pt, ct);
+            zero_part<T>(rowp, pt, ct);
             if (ct == 0 && rank == 0) {
                 P.loss[r] = 0.f;
                 if (P.ce_loss) P.ce_loss[r] = 0.f;
@@ -833,11 +835,9 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         cur.r = r;
         cur.rowp = rowp;
         cur.pt = pt;
-        cur.nt = (pt.bn + kTileF - 1) / kTileF;
+        cur.nt = (pt.bn + kTileE<T> - 1) / kTileE<T>;
         cur.inwin = inwin;
         cur.first = rank == 0;
-        cur.which = -1;
-        cur.j = -1;
         cur.jl = -1;
         cur.bad = false;
         if (has_label) {
@@ -877,24 +877,13 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                     S.ep[sb][q] = p;
                     scol[i] = col;
                     sp[i] = p;
-                    if (col >= 0) sx[i] = rowp[col];
+                    if (col >= 0) sx[i] = Elem<T>::get(rowp + col);
                 }
             }
         }
-        // KL loss parts of the support entries this thread holds: a = sum p (ln p - s),
-        // b = sum p (the loss is a + lse * b; entries with p <= 0 add no term)
-        float ka = 0.f, kb = 0.f;
-        if (kKL) {
-#pragma unroll
-            for (int i = 0; i < EPT; ++i)
-                if (scol[i] >= 0 && sp[i] > 0.f) {
-                    ka += sp[i] * (logf(sp[i]) - sx[i]);
-                    kb += sp[i];
-                }
-        }
-        cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
-        cur.jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
-        cur.ht = cur.has_ht ? rowp[cur.jht] : 0.f;
+        cur.has_ht = has_ht<T>(pt, ct);
+        cur.jht = ht_col<T>(pt, ct);
+        cur.ht = cur.has_ht ? Elem<T>::get(rowp + cur.jht) : 0.f;
 
         // ---- pass A: (max, sum) online over the streamed tiles
         MaxSum ms = ms_empty();
@@ -902,16 +891,13 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         for (int t = 0; t < cur.nt; ++t) {
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
             wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-            const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
-            float4 v[kVec];
+            const int n16 = min(kTileE<T>, pt.bn - t * kTileE<T>) / NV;
+            float v[kVec][NV];
 #pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                const int j = u * NCT + ct;
-                v[u] = j < n4 ? ld_shared_v4(&S.ring[slot][j * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
+            for (int u = 0; u < kVec; ++u) load_chunk<T>(S, slot, u * NCT + ct, n16, v[u]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
-            ms_addv(ms, v);
+            ms_addv<NV>(ms, v);
         }
         g += (uint32_t)cur.nt;
         ms = ms_warp_reduce(ms);
@@ -928,17 +914,29 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             }
             if (pend.r >= 0) {
                 collect(P, S, pend, ct);
-                pass_b<OP>(P, S, pend, g, ct, lane);
+                pass_b<T, OP>(P, S, pend, g, ct, lane);
             }
             pend = cur;
-            rk2 = rk1;
-            rk1 = r;
             ++li;
             continue;
         }
         const uint32_t b = nred & 1u;
         ++nred;
+        // KL loss parts of the support entries this thread holds: a = sum p (ln p - s),
+        // b = sum p (the loss is a + lse * b; entries with p <= 0 add no term).  Formed
+        // after pass A, so the gather of s overlaps the row's stream.
+        float ka = 0.f, kb = 0.f;
         if (kKL) {
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                if (scol[i] >= 0 && sp[i] > 0.f) {
+                    ka += sp[i] * (logf(sp[i]) - sx[i]);
+                    kb += sp[i];
+                }
+                // bf16: the logit kept for the support rewrite (exact: it is a bf16 value)
+                if (sizeof(T) == 2 && scol[i] >= 0)
+                    S.es[sb][ct + i * NCT] = (unsigned short)(__float_as_uint(sx[i]) >> 16);
+            }
             ka = warp_sum(ka);
             kb = warp_sum(kb);
         }
@@ -970,11 +968,26 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             }
         }
         // past this row's barrier, pass B of the row two back is done: its support terms
-        if (kKL && rk2 >= 0) scatter_support(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
+        if (kKL && rk2 >= 0) scatter_support<T>(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
+        // bf16: the label column of this row (slice coordinates; -1 none) for its rewrite
+        if (kKL && sizeof(T) == 2 && ct == LT) {
+            int jfull = -1;
+            if (has_label && !cur.bad) {
+                const long long j = (long long)lab_r - P.col0;
+                if (j >= 0 && j < ncols) jfull = (int)j;
+            }
+            S.erow[sb][2] = __int_as_float(jfull);
+        }
         // ---- pass B of the previous row
         if (pend.r >= 0) {
             if (c > 1) settle<OP>(P, S, pend, ct, rank);
-            pass_b<OP>(P, S, pend, g, ct, lane);
+            if (kKL && sizeof(T) == 2 && ct == 0) {
+                // bf16: the row statistics for its support rewrite, two rows on
+                const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
+                S.erow[pb][0] = pend.m;
+                S.erow[pb][1] = pend.lnS;
+            }
+            pass_b<T, OP>(P, S, pend, g, ct, lane);
         }
         pend = cur;
         rk2 = rk1;
@@ -984,174 +997,21 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     if (pend.r >= 0) {
         if (nobar) collect(P, S, pend, ct);
         else if (c > 1) settle<OP>(P, S, pend, ct, rank);
-        pass_b<OP>(P, S, pend, g, ct, lane);
+        if (kKL && sizeof(T) == 2 && ct == 0) {
+            const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
+            S.erow[pb][0] = pend.m;
+            S.erow[pb][1] = pend.lnS;
+        }
+        pass_b<T, OP>(P, S, pend, g, ct, lane);
     }
     if (kKL && li > 0) {
         named_sync(kBarConsumers, NCT);
-        if (rk2 >= 0) scatter_support(P, S, rk2, (li - 2u) % kSupBufs, ct);
-        scatter_support(P, S, rk1, (li - 1u) % kSupBufs, ct);
+        if (rk2 >= 0) scatter_support<T>(P, S, rk2, (li - 2u) % kSupBufs, ct);
+        scatter_support<T>(P, S, rk1, (li - 1u) % kSupBufs, ct);
     }
 }
 
-// Tail split: the statistics of tail row w.j from every CTA's part of it, merged in CTA
-// order.  Each warp merges on its own (lane i takes parts i, i + 32, ...; a butterfly
-// leaves the same sum in every lane), so every warp of every CTA holding a part gets the
-// same bits.  Waits are bounded like every other wait.
-__device__ void merge_parts(const RowParams& P, Smem& S, Pending& w, int ct, int lane, int U, uint32_t epoch) {
-    const long long G = gridDim.x;
-    const long long TU = (P.ntok - (P.ntok / G) * G) * (long long)U;
-    const long long x0 = w.j * U, x1 = (w.j + 1) * U - 1;
-    const long long b0 = ((x0 + 1) * G - 1) / TU, b1 = ((x1 + 1) * G - 1) / TU;   // CTAs holding units x0, x1
-    MaxSum acc = ms_empty();
-    for (long long b = b0 + lane; b <= b1; b += 32) {
-        const long long lo = b * TU / G;
-        if (lo >= (b + 1) * TU / G) continue;       // a CTA with an empty range holds no part
-        const int which = lo / U == w.j ? 0 : 1;
-        const unsigned int* sl = ws_slot(P, b, which);
-        const long long t0 = clock64();
-        bool ok = true;
-        while (ld_acquire_u32(sl + 2) != epoch) {
-            if (S.abort) { ok = false; break; }
-            if (clock64() - t0 > P.wait_limit) {
-                S.abort = 1;
-                atomicOr(&g_watchdog, 1u);
-                ok = false;
-                break;
-            }
-        }
-        if (!ok) break;
-        float m, sum;
-        asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(m), "=f"(sum) : "l"(sl) : "memory");
-        acc = ms_merge(acc, MaxSum{m, sum});
-    }
-    acc = ms_warp_reduce(acc);
-    w.m = acc.m;
-    w.lnS = logf(acc.s);
-    if (w.first && ct == LT) {
-        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
-        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
-    }
-}
-
-// Self-contained CE with the tail split (one CTA per SM, no clusters): whole rows with
-// the barrier-free statistics of consumer_self, then up to two tail segments whose
-// statistics come from every CTA's part of their row.
-template <int OP>
-__device__ void consumer_split(const RowParams& P, Smem& S) {
-    const int ct = (int)threadIdx.x - 32;
-    const int cw = ct >> 5, lane = ct & 31;
-    const int ncols = (int)P.ncols;
-    const int U = (ncols + 3) >> 2;
-    const uint32_t epoch = ld_relaxed_u32(P.ws) + 1u;
-    // barrier-free statistics need a body tile in every row (the ring then keeps the
-    // warps within kPartBufs rows of each other); shorter rows take the barrier
-    const bool nobar = ncols >= 8;
-    uint32_t g = 0, na = 0, nb = 0;
-    Pending pend;
-    pend.r = -1;
-    Item nxt;
-    bool have = item_at(P, 0, U, nxt);
-    uint32_t nlab = have ? P.labels[nxt.r] : 0u;
-    for (long long i = 0; have; ++i) {
-        const Item it = nxt;
-        const uint32_t lab_r = nlab;
-        have = item_at(P, i + 1, U, nxt);
-        if (have) nlab = P.labels[nxt.r];
-        float* rowp = P.x + it.r * P.ld + P.col0;
-        const Part pt = part_units(rowp, ncols, U, it.u0, it.u1);
-        Pending cur;
-        cur.r = it.r;
-        cur.rowp = rowp;
-        cur.pt = pt;
-        cur.nt = (pt.bn + kTileF - 1) / kTileF;
-        cur.inwin = it.r >= P.ls && it.r < P.le;
-        cur.first = it.u0 == 0;
-        cur.which = it.which;
-        cur.j = it.j;
-        cur.jl = -1;
-        cur.bad = (long long)lab_r >= P.V;
-        if (!cur.bad) {
-            const long long jj = (long long)lab_r - P.col0;
-            if (jj >= pt.lo && jj < pt.hi) cur.jl = (int)jj;
-        }
-        if (cur.bad && cur.inwin && cur.first && ct == LT && P.err) atomicAdd(P.err, 1);
-        cur.has_ht = ct < pt.hn || (ct >= 4 && ct - 4 < pt.tn);
-        cur.jht = ct < pt.hn ? ct : pt.t0 + ct - 4;
-        cur.ht = cur.has_ht ? rowp[cur.jht] : 0.f;
-
-        // ---- pass A
-        MaxSum ms = ms_empty();
-        if (cur.has_ht) ms_add(ms, cur.ht);
-        for (int t = 0; t < cur.nt; ++t) {
-            const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
-            wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-            const int n4 = min(kTileF, pt.bn - t * kTileF) >> 2;
-            float4 v[kVec];
-#pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                const int jv = u * NCT + ct;
-                v[u] = jv < n4 ? ld_shared_v4(&S.ring[slot][jv * 4]) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty[slot]);
-            ms_addv(ms, v);
-        }
-        g += (uint32_t)cur.nt;
-        ms = ms_warp_reduce(ms);
-        if (it.which < 0 && nobar) {
-            // a whole row: the warps' partials go through the mbarrier buffers
-            cur.ab = na % kPartBufs;
-            cur.apar = (na / kPartBufs) & 1u;
-            ++na;
-            if (lane == 0) {
-                S.wpart[cur.ab][cw] = make_float2(ms.m, ms.s);
-                mbar_arrive(&S.abar[cur.ab]);
-            }
-        } else {
-            const uint32_t b = nb & 1u;
-            ++nb;
-            if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, 0.f, 0.f);
-            named_sync(kBarConsumers, NCT);
-            const MaxSum tot = combine4(S.wred[b], NCW).ms;
-            if (it.which >= 0) {
-                // a tail segment: this CTA's part, published at once for the row's other parts
-                if (ct == 0) publish_part(P, it.which, tot, epoch);
-            } else {
-                cur.m = tot.m;
-                cur.lnS = logf(tot.s);
-                if (ct == LT) {
-                    if (P.lse_out) P.lse_out[it.r] = cur.m + cur.lnS;
-                    if (P.stats_out) { P.stats_out[2 * it.r] = cur.m; P.stats_out[2 * it.r + 1] = cur.lnS; }
-                }
-            }
-        }
-        if (pend.r >= 0) {
-            if (pend.which >= 0) merge_parts(P, S, pend, ct, lane, U, epoch);
-            else if (nobar) collect(P, S, pend, ct);
-            pass_b<OP>(P, S, pend, g, ct, lane);
-        }
-        pend = cur;
-    }
-    if (pend.r >= 0) {
-        if (pend.which >= 0) merge_parts(P, S, pend, ct, lane, U, epoch);
-        else if (nobar) collect(P, S, pend, ct);
-        pass_b<OP>(P, S, pend, g, ct, lane);
-    }
-}
-
-// Tail split: the last CTA to finish advances the workspace generation (every CTA has
-// read it at its start and is done with every slot by now).
-__device__ __forceinline__ void take_ticket(const RowParams& P) {
-    __threadfence();
-    const unsigned int t = atomicAdd(P.ws + 1, 1u);
-    if (t == gridDim.x - 1) {
-        P.ws[1] = 0u;
-        __threadfence();
-        atomicAdd(P.ws, 1u);
-    }
-}
-
-template <int OP, bool RES>
+template <typename T, int OP, bool RES>
 __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant__ RowParams P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -1166,7 +1026,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
             mbar_init(&S.empty[s], NCW);
         }
         for (int b = 0; b < 4; ++b) mbar_init(&S.xbar[b], 1u);   // the local expect_tx; the peers' data completes the bytes
-        for (int b = 0; b < 2; ++b) mbar_init(&S.lbar[b], 1u);
         for (int b = 0; b < kPartBufs; ++b) mbar_init(&S.abar[b], NCW);
         S.abort = 0;
         S.issued = 0;
@@ -1179,39 +1038,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
     pdl_wait_primary();
     pdl_launch_dependents();
 
-    const bool split = OP == kCeFused && P.split;
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
-            if (split) producer_split(P, S);
-            else producer<OP, RES>(P, S, rank, cid, ncl);
+            producer<T, OP, RES>(P, S, rank, cid, ncl);
             drain(S, P.wait_limit);
         }
         __syncwarp();
     } else {
-        if (split) consumer_split<OP>(P, S);
-        else if (RES) consumer_self<OP>(P, S, rank, cid, ncl);
-        else consumer<OP, false>(P, S, rank, cid, ncl);
+        if (RES) consumer_self<T, OP>(P, S, rank, cid, ncl);
+        else consumer<T, OP>(P, S, rank, cid, ncl);
     }
     // no CTA may leave while a peer can still write into its shared memory
     if (c > 1) cluster_sync_all();
-    if (split) {
-        __syncthreads();
-        if (threadIdx.x == 0) take_ticket(P);
-    }
 }
 
-const void* kernel_for(int op, bool res) {
+template <typename T>
+const void* kernel_for_t(int op, bool res) {
     switch (op) {
-        case kCeFused: return (const void*)row_kernel<kCeFused, true>;
-        case kCeFwd: return (const void*)row_kernel<kCeFwd, false>;
-        case kCeBwd: return (const void*)row_kernel<kCeBwd, false>;
-        case kKl: return res ? (const void*)row_kernel<kKl, true> : (const void*)row_kernel<kKl, false>;
+        case kCeFused: return (const void*)row_kernel<T, kCeFused, true>;
+        case kCeFwd: return (const void*)row_kernel<T, kCeFwd, false>;
+        case kCeBwd: return (const void*)row_kernel<T, kCeBwd, false>;
+        case kKl: return res ? (const void*)row_kernel<T, kKl, true> : (const void*)row_kernel<T, kKl, false>;
         default: return nullptr;
     }
 }
 
+const void* kernel_for(int op, bool res, int dtype) {
+    return dtype == kBf16 ? kernel_for_t<__nv_bfloat16>(op, res) : kernel_for_t<float>(op, res);
+}
+
 constexpr int kMaxDev = 64;
-std::atomic<int> g_attr_done[kMaxDev][8];
+constexpr int kFnSlots = 16;
+std::atomic<int> g_attr_done[kMaxDev][kFnSlots];
 
 cudaError_t prepare(const void* fn, int slot) {
     int dev = 0;
@@ -1225,14 +1083,14 @@ cudaError_t prepare(const void* fn, int slot) {
     return cudaSuccess;
 }
 
-int slot_of(int op, bool res) { return op * 2 + (res ? 1 : 0); }
+int slot_of(int op, bool res, int dtype) { return (dtype == kBf16 ? 8 : 0) + op * 2 + (res ? 1 : 0); }
 
 }  // namespace
 
 cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters, cudaStream_t st) {
-    const void* fn = kernel_for(op, resident);
+    const void* fn = kernel_for(op, resident, P.dtype);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = prepare(fn, slot_of(op, resident));
+    cudaError_t e = prepare(fn, slot_of(op, resident, P.dtype));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * P.csize), 1, 1);
@@ -1258,11 +1116,11 @@ cudaError_t launch_rows(int op, bool resident, const RowParams& P, int nclusters
 
 // Occupancy answers per (device, kernel, cluster size), queried once: the query costs
 // tens of microseconds, far more than a launch.
-std::atomic<int> g_max_clusters[kMaxDev][8][kMaxCluster + 1];
+std::atomic<int> g_max_clusters[kMaxDev][kFnSlots][kMaxCluster + 1];
 
-int row_max_clusters(int op, bool resident, int c) {
-    const void* fn = kernel_for(op, resident);
-    const int slot = slot_of(op, resident);
+int row_max_clusters(int op, bool resident, int c, int dtype) {
+    const void* fn = kernel_for(op, resident, dtype);
+    const int slot = slot_of(op, resident, dtype);
     if (!fn || c < 1 || c > kMaxCluster || prepare(fn, slot) != cudaSuccess) return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;

@@ -31,6 +31,7 @@
 //     their bucket, and the first k written with their probabilities.
 #include "vl_device.cuh"
 #include "vl_internal.h"
+#include "vl_topk.cuh"
 
 #include <atomic>
 
@@ -89,32 +90,21 @@ struct alignas(128) TSmem {
 
 static_assert(sizeof(TSmem) <= 227 * 1024, "shared memory of one CTA");
 
-__device__ __forceinline__ uint32_t f2key(float x) {
-    uint32_t b = __float_as_uint(x);
-    if (b == 0x80000000u) b = 0u;                      // -0.0 ranks as +0.0
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-__device__ __forceinline__ float key2f(uint32_t k) {
-    return (k & 0x80000000u) ? __uint_as_float(k & 0x7fffffffu) : __uint_as_float(~k);
-}
-
-// composite order on (key, id): larger key first, then lower id
-__device__ __forceinline__ unsigned long long comp(uint32_t key, uint32_t id) {
-    return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - id);
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
 // ---------------------------------------------------------------- producer
 
-__device__ void producer(const float* x, long long ld, long long V, long long ls, long long le, TSmem& S) {
+// Rows of a launch: [ls, le), or the `nlist` rows of `list` (the rows a filtered launch
+// could not finish).
+struct Rows {
+    long long ls;
+    long long n;
+    const int* list;
+    __device__ __forceinline__ long long at(long long i) const { return list ? (long long)list[i] : ls + i; }
+};
+
+__device__ void producer(const float* x, long long ld, long long V, const Rows& R, TSmem& S) {
     uint32_t g = 0;
-    for (long long r = ls + (long long)blockIdx.x; r < le; r += gridDim.x) {
+    for (long long i = blockIdx.x; i < R.n; i += gridDim.x) {
+        const long long r = R.at(i);
         const float* rowp = x + r * ld;
         const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
         int h = (4 - mis) & 3;
@@ -479,32 +469,6 @@ __device__ __forceinline__ void admit(TSmem& S, RowState& st, const float4 (&v)[
     }
 }
 
-// This warp's a-th largest of its values of the first tile (kVecT float4s a lane, all
-// present): a rounds of taking the warp's largest out.
-__device__ __forceinline__ float warp_kth(float4 (&v)[kVecT], uint32_t a, int lane) {
-    float e[4 * kVecT];
-#pragma unroll
-    for (int u = 0; u < kVecT; ++u) { e[4 * u] = v[u].x; e[4 * u + 1] = v[u].y; e[4 * u + 2] = v[u].z; e[4 * u + 3] = v[u].w; }
-    float top = -INFINITY;
-    for (uint32_t i = 0; i < a; ++i) {
-        float m = e[0];
-#pragma unroll
-        for (int q = 1; q < 4 * kVecT; ++q) m = fmaxf(m, e[q]);
-        top = m;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
-        // the lowest lane holding it takes one copy out
-        const uint32_t holders = __ballot_sync(0xffffffffu, m == top);
-        if (lane == __ffs(holders) - 1) {
-            bool done = false;
-#pragma unroll
-            for (int q = 0; q < 4 * kVecT; ++q)
-                if (!done && e[q] == top) { e[q] = -INFINITY; done = true; }
-        }
-    }
-    return top;
-}
-
 // The end of a row, all warps: at most K + SLACK survivors, ordered by (value desc, id asc)
 // through 2048 buckets of the key range, the first K written with their probabilities.
 // Returns false, doing nothing, when the row ran with a speculative threshold that
@@ -629,7 +593,7 @@ __device__ __noinline__ bool finish_row(TSmem& S, uint32_t K, int ct, const RowS
 
 // ---------------------------------------------------------------- consumer
 
-__device__ void consumer(const float* x, long long ld, long long V, int k, long long ls, long long le,
+__device__ void consumer(const float* x, long long ld, long long V, int k, const Rows& R,
                          uint32_t* ids, float* probs, int* err, TSmem& S) {
     const int ct = (int)threadIdx.x - 32;
     const int cw = ct >> 5, lane = ct & 31;
@@ -638,7 +602,8 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
     const uint32_t trig = max(4u * K, 1024u);                               // total that asks for a cut
     volatile int* need = &S.need;
     uint32_t g = 0;
-    for (long long r = ls + (long long)blockIdx.x; r < le; r += gridDim.x) {
+    for (long long i = blockIdx.x; i < R.n; i += gridDim.x) {
+        const long long r = R.at(i);
         const float* rowp = x + r * ld;
         const int mis = (int)((reinterpret_cast<uintptr_t>(rowp) >> 2) & 3u);
         int h = (4 - mis) & 3;
@@ -776,7 +741,7 @@ __device__ void consumer(const float* x, long long ld, long long V, int k, long 
 
 __global__ void __maxnreg__(128)
 topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long long ls, long long le,
-            uint32_t* __restrict__ ids, float* __restrict__ probs, int* err) {
+            const int* list, const int* nlist, uint32_t* __restrict__ ids, float* __restrict__ probs, int* err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     TSmem& S = *reinterpret_cast<TSmem*>(smem_raw);
     if (threadIdx.x == 0) {
@@ -797,14 +762,15 @@ topk_kernel(const float* __restrict__ x, long long ld, long long V, int k, long 
     // previous kernel on the stream; its results are visible past this wait
     pdl_wait_primary();
     pdl_launch_dependents();
+    const Rows R{ls, list ? (long long)*nlist : le - ls, list};
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
-            producer(x, ld, V, ls, le, S);
+            producer(x, ld, V, R, S);
             drain(S);
         }
         __syncwarp();
     } else {
-        consumer(x, ld, V, k, ls, le, ids, probs, err, S);
+        consumer(x, ld, V, k, R, ids, probs, err, S);
     }
 }
 
@@ -813,7 +779,8 @@ std::atomic<int> g_attr_done[64];
 }  // namespace
 
 cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long V, int k, long long ls,
-                        long long le, uint32_t* ids, float* probs, int* err, cudaStream_t st) {
+                        long long le, const int* list, const int* nlist, uint32_t* ids, float* probs, int* err,
+                        cudaStream_t st) {
     (void)ntok;
     if (k < 1 || k > KMAXT) return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
@@ -846,7 +813,7 @@ cudaError_t launch_topk(const float* x, long long ld, long long ntok, long long 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_kernel, x, ld, V, k, ls, le, ids, probs, err);
+    return cudaLaunchKernelEx(&cfg, topk_kernel, x, ld, V, k, ls, le, list, nlist, ids, probs, err);
 }
 
 unsigned int topk_watchdog(bool clear) {

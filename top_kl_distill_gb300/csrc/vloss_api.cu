@@ -96,7 +96,7 @@ int l2_bytes() {
     return v;
 }
 
-Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
+Grid choose_grid(int op, bool resident, long long rows, long long ncols, int dtype) {
     const int sms = num_sms();
     if (!resident) {
         long long g = rows < sms ? rows : sms;
@@ -105,7 +105,7 @@ Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
     // Self-contained mode re-reads a row part in pass B from L2 while the next part is
     // read: about two parts of 4 ncols / c bytes per CTA are live.  Splitting a row over
     // c CTAs keeps them within a third of L2 (c = 4 at 128256 columns on a GB300).
-    const double live = 2.0 * 4.0 * (double)ncols * (double)sms;
+    const double live = 2.0 * (dtype == kBf16 ? 2.0 : 4.0) * (double)ncols * (double)sms;
     const double budget = l2_bytes() > 0 ? l2_bytes() / 3.0 : 40e6;
     int cmin = 1;
     while (cmin < kMaxCluster && live / cmin > budget) ++cmin;
@@ -114,18 +114,19 @@ Grid choose_grid(int op, bool resident, long long rows, long long ncols) {
         return e ? std::atoi(e) : 0;
     }();
     if (forced >= 1 && forced <= kMaxCluster) {
-        const int n = row_max_clusters(op, resident, forced);
+        const int n = row_max_clusters(op, resident, forced, dtype);
         if (n > 0) return Grid{forced, (int)(rows < n ? rows : n)};
     }
-    const double exchange = 4.0 * kTileF;
+    const double esize = dtype == kBf16 ? 2.0 : 4.0;
+    const double exchange = 4.0 * kTileB;          // modelled fixed cost of a cluster exchange, in bytes
     Grid best{0, 0};
     double best_cost = 0;
     for (int c = cmin; c <= kMaxCluster; ++c) {
-        const int n = row_max_clusters(op, resident, c);
+        const int n = row_max_clusters(op, resident, c, dtype);
         if (n <= 0) continue;
         const long long ncl = rows < n ? rows : n;
         const long long waves = (rows + ncl - 1) / ncl;
-        const double cost = (double)waves * ((double)((ncols + c - 1) / c) + (c > 1 ? exchange : 0.0));
+        const double cost = (double)waves * ((double)((ncols + c - 1) / c) * esize + (c > 1 ? exchange : 0.0));
         if (best.csize == 0 || cost < best_cost * 0.98) {
             best = Grid{c, (int)(ncl > 0 ? ncl : 1)};
             best_cost = cost;
@@ -230,10 +231,11 @@ cudaError_t launch_mean(const float* loss, long long ls, long long le, float* me
     return cudaLaunchKernelExC(&cfg, (const void*)mean_kernel, args);
 }
 
-RowParams base_params(float* logits, int64_t ld, int64_t ntok, int64_t V) {
+RowParams base_params(const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V) {
     RowParams P;
     std::memset(&P, 0, sizeof(P));
-    P.x = logits;
+    P.x = const_cast<void*>(logits);
+    P.dtype = dtype;
     P.ld = ld;
     P.ntok = ntok;
     P.V = V;
@@ -251,7 +253,7 @@ thread_local long long g_inject_withhold = -1;
 thread_local long long g_inject_wait = 0;
 
 vl_status run_rows(int op, bool resident, RowParams& P, long long rows, const char* fn, cudaStream_t st) {
-    const Grid g = choose_grid(op, resident, rows, P.ncols);
+    const Grid g = choose_grid(op, resident, rows, P.ncols, P.dtype);
     if (g.csize == 0) return fail(VL_ELAUNCH, "%s: no launch configuration fits this device", fn);
     P.csize = g.csize;
     if (g_inject_wait > 0) {
@@ -261,21 +263,6 @@ vl_status run_rows(int op, bool resident, RowParams& P, long long rows, const ch
         g_inject_wait = 0;
     }
     const cudaError_t e = launch_rows(op, resident, P, g.nclusters, st);
-    if (e != cudaSuccess) return cuda_fail(e, fn);
-    return ok();
-}
-
-// The tail-split launch of the fused CE kernel: one CTA per SM.
-vl_status run_split(RowParams& P, int sms, const char* fn, cudaStream_t st) {
-    if (row_max_clusters(kCeFused, true, 1) <= 0) return fail(VL_ELAUNCH, "%s: the row kernel does not fit", fn);
-    P.csize = 1;
-    if (g_inject_wait > 0) {
-        P.withhold = g_inject_withhold;
-        P.wait_limit = g_inject_wait;
-        g_inject_withhold = -1;
-        g_inject_wait = 0;
-    }
-    const cudaError_t e = launch_rows(kCeFused, true, P, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
 }
@@ -301,17 +288,16 @@ const char* vl_status_string(vl_status s) {
 
 const char* vl_last_error_string(void) { return g_last_error.c_str(); }
 
-vl_status vl_ce_fwd(const float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+static vl_status ce_fwd_impl(const char* fn, const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
                     int64_t loss_start, int64_t loss_end, float* loss, float* lse, float* stats, float* mean,
                     int32_t* err, void* stream) {
-    const char* fn = "vl_ce_fwd";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
     if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
     const cudaStream_t st = as_stream(stream);
     if (ntok > 0) {
-        RowParams P = base_params(const_cast<float*>(logits), ld, ntok, V);
+        RowParams P = base_params(logits, dtype, ld, ntok, V);
         P.labels = labels;
         P.ls = loss_start;
         P.le = loss_end;
@@ -328,10 +314,9 @@ vl_status vl_ce_fwd(const float* logits, int64_t ld, int64_t ntok, int64_t V, co
     return VL_OK;
 }
 
-vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+static vl_status ce_bwd_impl(const char* fn, const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
                             const uint32_t* labels, const float* lse, const float* stats, int64_t loss_start,
                             int64_t loss_end, float scale, float* loss_part, int32_t* err, void* stream) {
-    const char* fn = "vl_ce_bwd_inplace";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
@@ -339,7 +324,7 @@ vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, 
     if (ntok > 0 && labels == nullptr) return fail(VL_EINVAL, "%s: labels is NULL", fn);
     if (ntok > 0 && lse == nullptr && stats == nullptr) return fail(VL_EINVAL, "%s: need lse or stats", fn);
     if (ntok == 0 || ncols == 0) return VL_OK;
-    RowParams P = base_params(logits, ld, ntok, V);
+    RowParams P = base_params(logits, dtype, ld, ntok, V);
     P.col0 = col0;
     P.ncols = ncols;
     P.labels = labels;
@@ -354,34 +339,16 @@ vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, 
     return run_rows(kCeBwd, false, P, ntok, fn, as_stream(stream));
 }
 
-vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+static vl_status ce_fused_impl(const char* fn, const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
                       int64_t loss_start, int64_t loss_end, float scale, float* loss, float* lse, float* stats,
-                      float* mean, int32_t* err, void* workspace, void* stream) {
-    const char* fn = "vl_ce_fused";
+                      float* mean, int32_t* err, void* stream) {
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
     if (ntok > 0 && (labels == nullptr || loss == nullptr)) return fail(VL_EINVAL, "%s: labels or loss is NULL", fn);
-    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return fail(VL_EINVAL, "%s: workspace not 16-byte aligned", fn);
     const cudaStream_t st = as_stream(stream);
-    const int sms = num_sms();
-    // the tail split pays off when the rows do not fill whole waves of the SMs
-    if (ntok > 0 && workspace && sms > 0 && ntok % sms != 0 && ws_bytes_for(sms) <= VL_WORKSPACE_BYTES) {
-        RowParams P = base_params(logits, ld, ntok, V);
-        P.labels = labels;
-        P.ls = loss_start;
-        P.le = loss_end;
-        P.cg = scale;
-        P.ce_coef = scale;
-        P.loss = loss;
-        P.lse_out = lse;
-        P.stats_out = stats;
-        P.err = err;
-        P.ws = static_cast<unsigned int*>(workspace);
-        P.split = 1;
-        if ((s = run_split(P, sms, fn, st))) return s;
-    } else if (ntok > 0) {
-        RowParams P = base_params(logits, ld, ntok, V);
+    if (ntok > 0) {
+        RowParams P = base_params(logits, dtype, ld, ntok, V);
         P.labels = labels;
         P.ls = loss_start;
         P.le = loss_end;
@@ -400,11 +367,10 @@ vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const 
     return VL_OK;
 }
 
-vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+static vl_status kl_impl(const char* fn, const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
                              const uint32_t* tid, const float* tp, int64_t k, float coef, int64_t loss_start,
                              int64_t loss_end, const float* lse_in, const float* stats_in, const uint32_t* labels,
                              float ce_coef, float* loss, int32_t* err, void* stream) {
-    const char* fn = "vl_kl_topk_inplace";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
@@ -417,7 +383,7 @@ vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
     if (self && (col0 != 0 || ncols != V))
         return fail(VL_EINVAL, "%s: a slice needs lse_in or stats_in (the statistics of the full row)", fn);
     if (ntok == 0) return VL_OK;
-    RowParams P = base_params(logits, ld, ntok, V);
+    RowParams P = base_params(logits, dtype, ld, ntok, V);
     P.col0 = col0;
     P.ncols = ncols;
     P.tid = tid;
@@ -438,11 +404,10 @@ vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V,
     return run_rows(kKl, self, P, rows > 0 ? rows : 1, fn, as_stream(stream));
 }
 
-vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+static vl_status ce_kl_impl(const char* fn, const void* logits, int dtype, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
                          const uint32_t* tid, const float* tp, int64_t k, float coef, float ce_coef,
                          int64_t loss_start, int64_t loss_end, float* kl_loss, float* ce_loss, float* lse,
                          float* stats, float* ce_mean, int32_t* err, void* stream) {
-    const char* fn = "vl_ce_kl_fused";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
     if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
@@ -453,7 +418,7 @@ vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, con
         return fail(VL_EINVAL, "%s: labels, tid, tp, kl_loss or ce_loss is NULL", fn);
     const cudaStream_t st = as_stream(stream);
     if (ntok > 0) {
-        RowParams P = base_params(logits, ld, ntok, V);
+        RowParams P = base_params(logits, dtype, ld, ntok, V);
         P.tid = tid;
         P.tp = tp;
         P.k = (int)k;
@@ -478,8 +443,101 @@ vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, con
     return VL_OK;
 }
 
+vl_status vl_ce_fwd(const float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                    int64_t loss_start, int64_t loss_end, float* loss, float* lse, float* stats, float* mean,
+                    int32_t* err, void* stream) {
+    return ce_fwd_impl("vl_ce_fwd", logits, kF32, ld, ntok, V, labels, loss_start, loss_end, loss, lse, stats,
+                       mean, err, stream);
+}
+
+vl_status vl_ce_fwd_bf16(const uint16_t* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                    int64_t loss_start, int64_t loss_end, float* loss, float* lse, float* stats, float* mean,
+                    int32_t* err, void* stream) {
+    return ce_fwd_impl("vl_ce_fwd_bf16", logits, kBf16, ld, ntok, V, labels, loss_start, loss_end, loss, lse,
+                       stats, mean, err, stream);
+}
+
+vl_status vl_ce_bwd_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                            const uint32_t* labels, const float* lse, const float* stats, int64_t loss_start,
+                            int64_t loss_end, float scale, float* loss_part, int32_t* err, void* stream) {
+    return ce_bwd_impl("vl_ce_bwd_inplace", logits, kF32, ld, ntok, V, col0, ncols, labels, lse, stats, loss_start,
+                       loss_end, scale, loss_part, err, stream);
+}
+
+vl_status vl_ce_bwd_inplace_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                            const uint32_t* labels, const float* lse, const float* stats, int64_t loss_start,
+                            int64_t loss_end, float scale, float* loss_part, int32_t* err, void* stream) {
+    return ce_bwd_impl("vl_ce_bwd_inplace_bf16", logits, kBf16, ld, ntok, V, col0, ncols, labels, lse, stats,
+                       loss_start, loss_end, scale, loss_part, err, stream);
+}
+
+vl_status vl_ce_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                      int64_t loss_start, int64_t loss_end, float scale, float* loss, float* lse, float* stats,
+                      float* mean, int32_t* err, void* stream) {
+    return ce_fused_impl("vl_ce_fused", logits, kF32, ld, ntok, V, labels, loss_start, loss_end, scale, loss, lse,
+                         stats, mean, err, stream);
+}
+
+vl_status vl_ce_fused_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                      int64_t loss_start, int64_t loss_end, float scale, float* loss, float* lse, float* stats,
+                      float* mean, int32_t* err, void* stream) {
+    return ce_fused_impl("vl_ce_fused_bf16", logits, kBf16, ld, ntok, V, labels, loss_start, loss_end, scale, loss,
+                         lse, stats, mean, err, stream);
+}
+
+vl_status vl_kl_topk_inplace(float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                             const uint32_t* tid, const float* tp, int64_t k, float coef, int64_t loss_start,
+                             int64_t loss_end, const float* lse_in, const float* stats_in, const uint32_t* labels,
+                             float ce_coef, float* loss, int32_t* err, void* stream) {
+    return kl_impl("vl_kl_topk_inplace", logits, kF32, ld, ntok, V, col0, ncols, tid, tp, k, coef, loss_start,
+                   loss_end, lse_in, stats_in, labels, ce_coef, loss, err, stream);
+}
+
+vl_status vl_kl_topk_inplace_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V, int64_t col0, int64_t ncols,
+                             const uint32_t* tid, const float* tp, int64_t k, float coef, int64_t loss_start,
+                             int64_t loss_end, const float* lse_in, const float* stats_in, const uint32_t* labels,
+                             float ce_coef, float* loss, int32_t* err, void* stream) {
+    return kl_impl("vl_kl_topk_inplace_bf16", logits, kBf16, ld, ntok, V, col0, ncols, tid, tp, k, coef,
+                   loss_start, loss_end, lse_in, stats_in, labels, ce_coef, loss, err, stream);
+}
+
+vl_status vl_ce_kl_fused(float* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                         const uint32_t* tid, const float* tp, int64_t k, float coef, float ce_coef,
+                         int64_t loss_start, int64_t loss_end, float* kl_loss, float* ce_loss, float* lse,
+                         float* stats, float* ce_mean, int32_t* err, void* stream) {
+    return ce_kl_impl("vl_ce_kl_fused", logits, kF32, ld, ntok, V, labels, tid, tp, k, coef, ce_coef, loss_start,
+                      loss_end, kl_loss, ce_loss, lse, stats, ce_mean, err, stream);
+}
+
+vl_status vl_ce_kl_fused_bf16(uint16_t* logits, int64_t ld, int64_t ntok, int64_t V, const uint32_t* labels,
+                         const uint32_t* tid, const float* tp, int64_t k, float coef, float ce_coef,
+                         int64_t loss_start, int64_t loss_end, float* kl_loss, float* ce_loss, float* lse,
+                         float* stats, float* ce_mean, int32_t* err, void* stream) {
+    return ce_kl_impl("vl_ce_kl_fused_bf16", logits, kBf16, ld, ntok, V, labels, tid, tp, k, coef, ce_coef,
+                      loss_start, loss_end, kl_loss, ce_loss, lse, stats, ce_mean, err, stream);
+}
+
+// SMs of the current device; without one, 256 (more than any current GPU has).
+static long long current_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+        cudaGetLastError();
+        return 256;
+    }
+    return sms;
+}
+
+int64_t vl_topk_workspace_bytes(int64_t ntok, int64_t V, int64_t k) {
+    if (ntok < 1 || V < 1 || V > kMaxCols || k < 1 || k > V || k > VL_TOPK_KMAX) return 0;
+    if (topk_filter_spec_a(V, (int)k) == 0) return 0;
+    const long long sms = current_sms();
+    return topk_ws_bytes(ntok, V, (int)k, ntok < sms ? ntok : sms);
+}
+
 vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k, int64_t loss_start,
-                       int64_t loss_end, uint32_t* ids, float* probs, int32_t* err, void* stream) {
+                       int64_t loss_end, uint32_t* ids, float* probs, int32_t* err, void* workspace,
+                       int64_t workspace_bytes, void* stream) {
     const char* fn = "vl_topk_rows";
     vl_status s = check_rows(logits, ld, ntok, V, fn);
     if (s) return s;
@@ -488,9 +546,98 @@ vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int64_t V,
     if (k > VL_TOPK_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_TOPK_KMAX);
     if (loss_end > loss_start && (ids == nullptr || probs == nullptr))
         return fail(VL_EINVAL, "%s: ids or probs is NULL", fn);
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return fail(VL_EINVAL, "%s: workspace not 16-byte aligned", fn);
     if (loss_end == loss_start) return VL_OK;
-    const cudaError_t e = launch_topk(logits, ld, ntok, V, (int)k, loss_start, loss_end, ids, probs, err,
-                                      as_stream(stream));
+    cudaError_t e;
+    if (workspace && topk_filter_spec_a(V, (int)k) > 0 &&
+        workspace_bytes >= topk_ws_bytes(loss_end - loss_start, V, (int)k, 1))
+        e = launch_topk_stream(logits, ld, V, (int)k, loss_start, loss_end, ids, probs, err, workspace,
+                               workspace_bytes, kWaitTimeoutCycles, as_stream(stream));
+    else
+        e = launch_topk(logits, ld, ntok, V, (int)k, loss_start, loss_end, nullptr, nullptr, ids, probs, err,
+                        as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
+int64_t vl_teacher_topk_workspace_bytes(int64_t rows, int64_t V, int64_t k) {
+    if (rows < 1 || V < 1 || V > kMaxCols || k < 1 || k > V || k > VL_TOPK_KMAX) return 0;
+    return teacher_ws_bytes(rows, V, (int)k);
+}
+
+int64_t vl_head_kl_workspace_bytes(int64_t rows, int64_t V) {
+    if (rows < 1 || V < 1 || V > kMaxCols) return 0;
+    return head_kl_ws_bytes(rows, V);
+}
+
+static vl_status check_head(const void* hidden, int64_t hs, const void* w, int64_t V, int64_t ntok, void* ws,
+                            const char* fn) {
+    if (ntok < 0 || hs < 8 || hs % 8 != 0) return fail(VL_EINVAL, "%s: need ntok >= 0 and hs a positive multiple of 8", fn);
+    if (V < 1 || V > kMaxCols) return fail(VL_EINVAL, "%s: V must be in [1, %lld]", fn, kMaxCols);
+    if (ntok > 0 && (hidden == nullptr || w == nullptr || ws == nullptr))
+        return fail(VL_EINVAL, "%s: hidden, w or workspace is NULL", fn);
+    if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(ws)) & 15u)
+        return fail(VL_EINVAL, "%s: hidden, w and workspace must be 16-byte aligned", fn);
+    return VL_OK;
+}
+
+vl_status vl_teacher_topk(const uint16_t* hidden, int64_t hs, const uint16_t* w, int64_t V, int64_t ntok, int64_t k,
+                          int64_t loss_start, int64_t loss_end, uint32_t* ids, float* probs, int32_t* err,
+                          void* workspace, int64_t workspace_bytes, void* stream) {
+    const char* fn = "vl_teacher_topk";
+    vl_status s = check_head(hidden, hs, w, V, ntok, workspace, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (k < 1 || k > V) return fail(VL_EINVAL, "%s: k = %lld outside [1, V]", fn, (long long)k);
+    if (k > VL_TOPK_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_TOPK_KMAX);
+    if (loss_end > loss_start && (ids == nullptr || probs == nullptr))
+        return fail(VL_EINVAL, "%s: ids or probs is NULL", fn);
+    if (loss_end == loss_start) return VL_OK;
+    char msg[400];
+    const int r = teacher_topk(hidden, hs, w, V, ntok, (int)k, loss_start, loss_end, ids, probs, err, workspace,
+                               workspace_bytes, as_stream(stream), msg, sizeof(msg));
+    if (r) return fail((vl_status)r, "%s: %s", fn, msg);
+    return VL_OK;
+}
+
+vl_status vl_head_kl(const uint16_t* hidden, int64_t hs, const uint16_t* w, const uint16_t* wt, int64_t V, int64_t ntok,
+                     const uint32_t* labels, const uint32_t* tid, const float* tp, int64_t k, float coef,
+                     float ce_coef, float dx_scale, int64_t loss_start, int64_t loss_end, float* dx, float* kl_loss,
+                     float* ce_loss, float* ce_mean, int32_t* err, void* workspace, int64_t workspace_bytes,
+                     void* stream) {
+    const char* fn = "vl_head_kl";
+    vl_status s = check_head(hidden, hs, w, V, ntok, workspace, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (k < 1) return fail(VL_EINVAL, "%s: k < 1", fn);
+    if (k > VL_KL_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_KL_KMAX);
+    if (ntok > 0 && (labels == nullptr || tid == nullptr || tp == nullptr || dx == nullptr || kl_loss == nullptr ||
+                     ce_loss == nullptr))
+        return fail(VL_EINVAL, "%s: labels, tid, tp, dx, kl_loss or ce_loss is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(dx) & 15u) return fail(VL_EINVAL, "%s: dx must be 16-byte aligned", fn);
+    if (ntok == 0) return VL_OK;
+    char msg[400];
+    if (wt && (reinterpret_cast<uintptr_t>(wt) & 15u)) return fail(VL_EINVAL, "%s: wt must be 16-byte aligned", fn);
+    const int r = head_kl(hidden, hs, w, wt, V, ntok, labels, tid, tp, (int)k, coef, ce_coef, dx_scale, loss_start,
+                          loss_end, dx, kl_loss, ce_loss, ce_mean, err, workspace, workspace_bytes,
+                          as_stream(stream), msg, sizeof(msg));
+    if (r) return fail((vl_status)r, "%s: %s", fn, msg);
+    return VL_OK;
+}
+
+vl_status vl_gemm_bf16_tn(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N, int64_t K,
+                          int64_t ldd, float alpha, void* stream) {
+    const char* fn = "vl_gemm_bf16_tn";
+    if (M < 0 || N < 0 || K < 0) return fail(VL_EINVAL, "%s: negative size", fn);
+    if (M == 0 || N == 0) return VL_OK;
+    if (K < 8 || K % 8 != 0) return fail(VL_EINVAL, "%s: K must be a positive multiple of 8", fn);
+    if (ldd < N) return fail(VL_EINVAL, "%s: ldd < N", fn);
+    if (A == nullptr || B == nullptr || D == nullptr) return fail(VL_EINVAL, "%s: NULL pointer", fn);
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
+        return fail(VL_EINVAL, "%s: A and B must be 16-byte aligned", fn);
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return fail(VL_EUNSUPPORTED, "%s: size above 2^30", fn);
+    const cudaError_t e = tc_gemm_tn(A, B, D, M, N, K, ldd, alpha, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return VL_OK;
 }
@@ -555,10 +702,11 @@ int vl_watchdog_flag(int device, int clear) {
         cudaSetDevice(prev);
         return -1;
     }
-    const unsigned int a = rows_watchdog(clear != 0), b = topk_watchdog(clear != 0);
+    const unsigned int a = rows_watchdog(clear != 0), b = topk_watchdog(clear != 0),
+                       c = topk_stream_watchdog(clear != 0), d = gemm_watchdog(clear != 0);
     cudaSetDevice(prev);
-    if (a == 0xffffffffu || b == 0xffffffffu) return -1;
-    return (int)((a | b) & 0x7fffffffu);
+    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu || d == 0xffffffffu) return -1;
+    return (int)((a | b | c | d) & 0x7fffffffu);
 }
 
 }  // extern "C"
