@@ -70,6 +70,7 @@ typedef enum vl_status {
 #define VL_KL_KMAX 1024      /* teacher support per row for vl_kl_topk_inplace */
 #define VL_TOPK_KMAX 2048    /* k of vl_topk_rows (the page's bound for topk_rows) */
 #define VL_MAX_COLS 0x7FFF0000LL   /* longest row V (2^31 - 2^16): rows are indexed with 32-bit ints */
+#define VL_TOPK_NOALLOC_BYTES (32ll << 20)   /* fixed scratch of vl_topk_rows_noalloc (32 MiB a device) */
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 VL_API int vl_version(void);
@@ -236,6 +237,29 @@ VL_API vl_status vl_topk_rows(const float* logits, int64_t ld, int64_t ntok, int
                        uint32_t* ids, float* probs, int32_t* err,
                        void* workspace, int64_t workspace_bytes, void* stream);
 
+/*
+ * vl_topk_rows for callers that cannot allocate device memory.  No counterpart on the
+ * pages: it is the same selection, with its scratch taken from a fixed array in the
+ * library instead of a workspace the caller passes.  It serves code that has no way to
+ * get device memory at the point of the call: a custom memory pool or allocator hook that
+ * calls into this library and must not re-enter the allocator, a latency-bound path that
+ * may not risk an allocation (or its failure) there, or an embedded runtime with no device
+ * allocator.  Results equal those of vl_topk_rows.
+ *   The scratch is one array of VL_TOPK_NOALLOC_BYTES (32 MiB) that every device which
+ *   loads the library holds until the process exits.  Rows of 30720 to 2^20 columns use
+ *   it (shorter or longer rows need no scratch).  A call takes at most as many rows of
+ *   the window as the array holds candidate regions and row list for (millions at
+ *   V = 128256; 97 at V = 2^20 and k = 2048 on a 152-SM device); a larger window is
+ *   rejected with VL_EUNSUPPORTED and a message that gives the limit (split it into calls).
+ *   The first call on a device looks up the array's device address there (with that
+ *   device current); make that first call before any stream capture.
+ *   Every call shares the one array, which keeps the last call's contents (what must start
+ *   at zero is cleared on the stream by each call); calls that overlap on the GPU -- on
+ *   two streams, or from two host threads -- race on it and give wrong results.
+ */
+VL_API vl_status vl_topk_rows_noalloc(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
+                               int64_t loss_start, int64_t loss_end,
+                               uint32_t* ids, float* probs, int32_t* err, void* stream);
 
 /*
  * Bytes of workspace with which vl_topk_rows streams ntok rows of V columns on one CTA per

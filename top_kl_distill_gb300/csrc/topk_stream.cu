@@ -33,6 +33,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <mutex>
 
 namespace vl {
 namespace {
@@ -540,6 +541,36 @@ cudaError_t launch_topk_stream(const float* x, long long ld, long long V, int k,
     if ((e = cudaLaunchKernelEx(&cfg, topk_stream_kernel, F)) != cudaSuccess) return e;
     // the rows the stream could not settle, exactly (NaN rows were counted already)
     return launch_topk(x, ld, le, V, k, ls, le, list, nlist, ids, probs, nullptr, st);
+}
+
+// ---------------------------------------------------------------- scratch without allocation
+//
+// For callers that cannot allocate device memory: the stream kernel's scratch in a fixed
+// array that every device loading the library holds until the process exits.  Host code
+// needs the array's device address (the symbol itself names a host-side stand-in); it is
+// looked up once per device, with that device current.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[VL_TOPK_NOALLOC_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+}  // namespace
+
+cudaError_t topk_noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
 }
 
 unsigned int topk_stream_watchdog(bool clear) {

@@ -68,6 +68,9 @@ cudaError_t launch_topk_stream(const float* x, long long ld, long long V, int k,
                                uint32_t* ids, float* probs, int* err, void* ws, long long ws_bytes,
                                long long wait_limit, cudaStream_t st);
 unsigned int topk_stream_watchdog(bool clear);
+// The device address of the fixed scratch array of vl_topk_rows_noalloc on the current
+// device (looked up once per device).
+cudaError_t topk_noalloc_scratch(void** out);
 
 // The head GEMM on the tensor cores (gemm.cu): D[M][N] (fp32, ldd) = alpha * A[M][K] . B[N][K]^T,
 // A and B bf16 row-major, 16-byte aligned, K a multiple of 8.

@@ -642,6 +642,55 @@ vl_status vl_gemm_bf16_tn(const uint16_t* A, const uint16_t* B, float* D, int64_
     return VL_OK;
 }
 
+// Scratch of a stream launch over `rows` rows with its full grid on the current device.
+static long long noalloc_need(long long rows, long long V, int k, long long sms) {
+    return topk_ws_bytes(rows, V, k, rows < sms ? rows : sms);
+}
+
+// The most rows one call takes with the fixed array (the need grows with the rows).
+static long long noalloc_max_rows(long long V, int k, long long sms) {
+    long long lo = 0, hi = 1LL << 40;
+    while (lo < hi) {
+        const long long mid = lo + (hi - lo + 1) / 2;
+        if (noalloc_need(mid, V, k, sms) <= VL_TOPK_NOALLOC_BYTES) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+vl_status vl_topk_rows_noalloc(const float* logits, int64_t ld, int64_t ntok, int64_t V, int64_t k,
+                               int64_t loss_start, int64_t loss_end, uint32_t* ids, float* probs, int32_t* err,
+                               void* stream) {
+    const char* fn = "vl_topk_rows_noalloc";
+    vl_status s = check_rows(logits, ld, ntok, V, fn);
+    if (s) return s;
+    if ((s = check_window(loss_start, loss_end, ntok, fn))) return s;
+    if (k < 1 || k > V) return fail(VL_EINVAL, "%s: k = %lld outside [1, V]", fn, (long long)k);
+    if (k > VL_TOPK_KMAX) return fail(VL_EUNSUPPORTED, "%s: k = %lld > %d", fn, (long long)k, VL_TOPK_KMAX);
+    if (loss_end > loss_start && (ids == nullptr || probs == nullptr))
+        return fail(VL_EINVAL, "%s: ids or probs is NULL", fn);
+    const long long rows = loss_end - loss_start;
+    if (rows == 0) return VL_OK;
+    cudaError_t e;
+    if (topk_filter_spec_a(V, (int)k) > 0) {
+        const long long sms = current_sms();
+        const long long need = noalloc_need(rows, V, (int)k, sms);
+        if (need > VL_TOPK_NOALLOC_BYTES)
+            return fail(VL_EUNSUPPORTED,
+                        "%s: %lld rows need %lld bytes of scratch, more than the fixed %lld; call it on at most "
+                        "%lld rows at a time",
+                        fn, rows, need, (long long)VL_TOPK_NOALLOC_BYTES, noalloc_max_rows(V, (int)k, sms));
+        void* scratch = nullptr;
+        if ((e = topk_noalloc_scratch(&scratch)) != cudaSuccess) return cuda_fail(e, fn);
+        e = launch_topk_stream(logits, ld, V, (int)k, loss_start, loss_end, ids, probs, err, scratch,
+                               VL_TOPK_NOALLOC_BYTES, kWaitTimeoutCycles, as_stream(stream));
+    } else {
+        e = launch_topk(logits, ld, ntok, V, (int)k, loss_start, loss_end, nullptr, nullptr, ids, probs, err,
+                        as_stream(stream));
+    }
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return VL_OK;
+}
+
 vl_status vl_window_mean(const float* loss, int64_t ntok, int64_t loss_start, int64_t loss_end, float* mean,
                          void* stream) {
     const char* fn = "vl_window_mean";

@@ -38,6 +38,7 @@ _SIGS = {
     "vl_ce_kl_fused": [_P, _I, _I, _I, _P, _P, _P, _I, _F, _F, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "vl_teacher_topk": [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P],
     "vl_gemm_bf16_tn": [_P, _P, _P, _I, _I, _I, _I, _F, _P],
+    "vl_topk_rows_noalloc": [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P],
     "vl_head_kl": [_P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _F, _F, _F, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P],
     "vl_ce_fwd_bf16": [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P],
     "vl_ce_bwd_inplace_bf16": [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P],
@@ -328,3 +329,11 @@ def vl_gemm_bf16_tn(A, B, D, M, N, K, ldd, alpha=1.0, stream=None):
     """D[M][N] = alpha * A[M][K] . B[N][K]^T on the tensor cores; A, B bf16, D fp32."""
     _check("vl_gemm_bf16_tn", lib().vl_gemm_bf16_tn(_ptr(A, "bf16", "A"), _ptr(B, "bf16", "B"), _ptr(D, "f32", "D"),
                                                     M, N, K, ldd, float(alpha), _stream(stream)))
+
+
+def vl_topk_rows_noalloc(logits, ld, ntok, V, k, loss_start, loss_end, ids, probs, err=None, stream=None):
+    """vl_topk_rows with the library's fixed scratch array instead of a workspace: for callers
+    that cannot allocate device memory at the point of the call (see include/vloss.h)."""
+    _check("vl_topk_rows_noalloc", lib().vl_topk_rows_noalloc(
+        _ptr(logits, "f32", "logits"), ld, ntok, V, k, loss_start, loss_end, _ptr(ids, "u32", "ids"),
+        _ptr(probs, "f32", "probs"), _ptr(err, "i32", "err"), _stream(stream)))
