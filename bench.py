@@ -181,6 +181,51 @@ class CeFused(Case):
         self.step(j, mean=False)
 
 
+class CeFusedShard(CeFused):
+    """This rank's contiguous row shard of the fused CE batch (dist.window_shard): the fused
+    kernel over its rows with its part of the loss window and the batch's gradient scale,
+    then the one exchange step, an all-reduce of (mean x rows) that gives every rank the
+    batch's mean over the window (dist.global_window_mean)."""
+
+    def __init__(self, torch, w, nbuf, rank, ws):
+        from top_kl_distill_gb300 import vloss as vl
+        from top_kl_distill_gb300.dist import window_shard
+        self.vl, self.torch = vl, torch
+        self.batch = w
+        r0, r1, ls, le = window_shard(w.ntok, rank, ws, w.loss_start, w.loss_end)
+        self.r0, self.r1, self.ls, self.le = r0, r1, ls, le
+        self.w = w
+        self.name = w.name
+        self.launches_per_step = 2
+        self.x_host = W.logits(w, r0, r1)
+        self.lab_host = W.labels(w, r0, r1)
+        self.pristine = _dev(torch, self.x_host)
+        self.labels = _dev(torch, self.lab_host)
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(nbuf)]
+        n = r1 - r0
+        self.loss = torch.zeros(max(n, 1), device="cuda")
+        self.lse = torch.zeros(max(n, 1), device="cuda")
+        self.mean = torch.zeros(1, device="cuda")
+        self.global_mean = None
+
+    def rows(self):
+        return self.r1 - self.r0
+
+    def bytes_per_step(self):
+        return self.rows() * (8 * self.w.V + 12) + (self.le - self.ls) * 4 + 4
+
+    def kernel_bytes(self):
+        return self.rows() * (8 * self.w.V + 12)
+
+    def step(self, j, mean=True):
+        from top_kl_distill_gb300.dist import global_window_mean
+        w, n = self.w, self.rows()
+        self.vl.vl_ce_fused(self.bufs[j], w.V, n, w.V, self.labels, self.ls, self.le, w.scale,
+                            self.loss, self.lse, None, self.mean if mean else None, None)
+        if mean:
+            self.global_mean = global_window_mean(self.mean, self.le - self.ls, w.loss_end - w.loss_start)
+
+
 class CeFusedBf16(CeFused):
     """The fused CE step on bf16 logits (the same draws rounded to bf16): vl_ce_fused_bf16,
     2 bytes an element each way."""
@@ -249,7 +294,7 @@ class TopK(Case):
         self.bufs = [self.x]
         self.ids = torch.zeros((w.ntok, k), dtype=torch.int32, device="cuda")
         self.probs = torch.zeros((w.ntok, k), device="cuda")
-        self.launches_per_step = 3 if vl.vl_topk_workspace_bytes(w.ntok, w.V, k) else 1
+        self.launches_per_step = 2 if vl.vl_topk_workspace_bytes(w.ntok, w.V, k) else 1
 
     def rows(self):
         return self.w.ntok
@@ -263,8 +308,8 @@ class TopK(Case):
         pass
 
     def step(self, j):
-        """One vl_topk_rows call: with the workspace, the filter, finish and exact-rows
-        kernels (the last one finds its list empty on these rows)."""
+        """One vl_topk_rows call: with the workspace, the streaming kernel (filter and
+        finish warps) and the exact kernel for the rows it leaves (none on these rows)."""
         w = self.w
         self.vl.vl_topk_rows(self.x, w.V, w.ntok, w.V, self.k, 0, w.ntok, self.ids, self.probs)
 
@@ -794,6 +839,9 @@ def main():
     ap.add_argument("--ntok", type=int, default=0, help="rows of a scaled-down workload (profiling only)")
     ap.add_argument("--bufs", type=int, default=0, help="work buffers per timing round (profiling only)")
     ap.add_argument("--no-oracle", action="store_true", help="skip the CPU baseline and the e2e leg")
+    ap.add_argument("--shard", action="store_true",
+                    help="split the fused CE batch into row shards over the N ranks (strong scaling) "
+                         "instead of a batch per rank")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_setup()
@@ -817,7 +865,13 @@ def main():
     def flush():
         flush_buf.fill_(1.0)
 
-    case = make_case(torch, args.workload, args.ntok or None, args.bufs or None)
+    shard = args.shard and base_workload(args.workload).kind == "ce" and not args.workload.endswith("_bf16")
+    if shard:
+        w0 = base_workload(args.workload)
+        w0 = w0.scaled(args.ntok) if args.ntok else w0
+        case = CeFusedShard(torch, w0, args.bufs or nbuf_for(w0.ntok * w0.V * 4 // ws), rank, ws)
+    else:
+        case = make_case(torch, args.workload, args.ntok or None, args.bufs or None)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.3)
@@ -840,19 +894,21 @@ def main():
                         f"timed steps and {soak_rounds} further untimed rounds of the same step")
 
     ms_step = total_ms / args.steps
-    rows_all = case.rows() * ws
+    rows_all = case.batch.ntok if shard else case.rows() * ws
     value = rows_all / (ms_step * 1e-3)
     kernel_ms = k_ms_total / args.steps
     e2e_ms, h2d, d2h, e2e_ok = (None, 0, 0, None)
-    if isinstance(case, CeFused) and not args.no_oracle:
+    if isinstance(case, CeFused) and not shard and not args.no_oracle:
         e2e_ms, h2d, d2h, e2e_ok = e2e_ce(torch, case, max(10, args.steps // 4), 3)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "strong" if shard else "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy, uploaded once)",
         "config": {"workload": workload_desc(case.w), "ntok": case.w.ntok, "V": case.w.V,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "parallelism": (f"row shards x{ws}, one all-reduce of the window mean a step" if shard
+                                   else f"replicas x{ws}" if ws > 1 else "single GPU"),
                    "l2": "fresh input copy per step; a 512 MB write flushes L2 before each group of timed steps",
                    "work_buffers": len(case.bufs)},
         "hbm_gbs_step": round(case.bytes_per_step() / (ms_step * 1e-3) / 1e9, 1),

@@ -314,7 +314,7 @@ template <typename T, int OP, bool RES>
 __device__ void producer(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     uint32_t g = 0;
     long long prev = -1;
-    for (long long r = cid; r < P.ntok; r += ncl) {
+    for (long long r = P.rbeg + cid; r < P.rend; r += ncl) {
         if (!row_loaded<OP>(P, r)) continue;
         if (!issue_part<T>(P, S, r, rank, g)) break;
         if (RES) {
@@ -435,13 +435,13 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
     uint32_t nlab = 0, nid = 0;
     float np = 0.f;
     auto prefetch = [&](long long rr) {
-        if (rr >= P.ntok) return;
+        if (rr >= P.rend) return;
         if (has_label) nlab = P.labels[rr];
         if (kKL && ct < P.k) { nid = P.tid[rr * P.k + ct]; np = P.tp[rr * P.k + ct]; }
     };
-    prefetch(cid);
+    prefetch(P.rbeg + cid);
 
-    for (long long r = cid; r < P.ntok; r += ncl) {
+    for (long long r = P.rbeg + cid; r < P.rend; r += ncl) {
         const uint32_t lab_r = nlab, id0 = nid;
         const float p0 = np;
         prefetch(r + ncl);
@@ -807,15 +807,15 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     uint32_t nlab = 0, nid = 0;
     float np = 0.f;
     auto prefetch = [&](long long rr) {
-        if (rr >= P.ntok) return;
+        if (rr >= P.rend) return;
         if (has_label) nlab = P.labels[rr];
         if (kKL && ct < P.k) { nid = P.tid[rr * P.k + ct]; np = P.tp[rr * P.k + ct]; }
     };
-    prefetch(cid);
+    prefetch(P.rbeg + cid);
     Pending pend;
     pend.r = -1;
 
-    for (long long r = cid; r < P.ntok; r += ncl) {
+    for (long long r = P.rbeg + cid; r < P.rend; r += ncl) {
         const uint32_t lab_r = nlab, id0 = nid;
         const float p0 = np;
         prefetch(r + ncl);

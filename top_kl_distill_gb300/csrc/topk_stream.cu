@@ -160,6 +160,56 @@ __device__ __forceinline__ void admit(uint2* out, uint32_t capw, uint32_t& wcnt,
     wcnt += (uint32_t)__popc(bal);
 }
 
+// max with NaN propagation (max.NaN): a NaN among the operands gives NaN.
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Admit this lane's 8 values of a tile (float4 u at columns cu[u] .. cu[u] + 3) that reach T
+// to the warp's region, all lanes at once: the lane's count c (0..8) in four bit planes, one
+// ballot per plane gives every lane its slot offset (the lanes below it) and the warp's
+// total; then each lane stores its values in column order.  A lane whose slots would pass
+// capw stores nothing (the warp's count passes capw: the row goes to the exact kernel).
+__device__ __forceinline__ void admit8(uint2* out, uint32_t capw, uint32_t& wcnt, float& wmax, bool& nan,
+                                       const float4 (&v)[FVEC], const uint32_t (&cu)[FVEC], const bool (&act)[FVEC],
+                                       float T, uint64_t pol) {
+    static_assert(FVEC == 2, "8 values a lane: four bit planes");
+    const float e[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+    bool k[8];
+    uint32_t c = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        k[q] = act[q >> 2] && e[q] >= T;        // slots past the row's body hold -inf, which T = -inf admits
+        c += k[q] ? 1u : 0u;
+    }
+    float mx = e[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) mx = max_nan(mx, e[q]);
+    nan |= mx != mx;
+    if (!__any_sync(0xffffffffu, c != 0)) return;
+    const uint32_t lt = lanemask_lt();
+    const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u);
+    const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
+    uint32_t pos = wcnt + (uint32_t)__popc(b0 & lt) + ((uint32_t)__popc(b1 & lt) << 1) +
+                   ((uint32_t)__popc(b2 & lt) << 2) + ((uint32_t)__popc(b3 & lt) << 3);
+    wcnt += __reduce_add_sync(0xffffffffu, c);
+    if (c != 0) wmax = fmaxf(wmax, mx);          // mx is NaN only with a NaN here; fmaxf skips it
+    if (c != 0 && pos + c <= capw) {
+        uint2* o = out + pos;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (k[q]) {
+                asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;"
+                             :: "l"(o), "r"(__float_as_uint(e[q])), "r"(cu[q >> 2] + (uint32_t)(q & 3)), "l"(pol)
+                             : "memory");
+                ++o;
+            }
+        }
+    }
+}
+
 // The filter warps never leave a barrier out: a wait that gave up (the CTA's abort flag is
 // then set and every later wait returns at once) is followed by the same steps on whatever
 // the buffers hold, and the host reports the watchdog.
@@ -215,21 +265,14 @@ __device__ void filter_warps(const StreamParams& F, KSmem& S) {
                     admit(out, capw, wcnt, wmax, keep && hv >= T, hv, id, keep_pol);
                 }
             }
+            uint32_t cu[FVEC];
+            bool act[FVEC];
 #pragma unroll
             for (int u = 0; u < FVEC; ++u) {
-                const int j = u * FT + ct;
-                const bool active = j < n4;
-                const float s4 = (v[u].x + v[u].y) + (v[u].z + v[u].w);
-                if (active && s4 != s4) nan |= isnan(v[u].x) || isnan(v[u].y) || isnan(v[u].z) || isnan(v[u].w);
-                const bool any = active && fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)) >= T;
-                if (__any_sync(0xffffffffu, any)) {
-                    const uint32_t c0 = (uint32_t)(h + t * FTILE + 4 * j);
-                    admit(out, capw, wcnt, wmax, any && v[u].x >= T, v[u].x, c0, keep_pol);
-                    admit(out, capw, wcnt, wmax, any && v[u].y >= T, v[u].y, c0 + 1, keep_pol);
-                    admit(out, capw, wcnt, wmax, any && v[u].z >= T, v[u].z, c0 + 2, keep_pol);
-                    admit(out, capw, wcnt, wmax, any && v[u].w >= T, v[u].w, c0 + 3, keep_pol);
-                }
+                cu[u] = (uint32_t)(h + t * FTILE + 4 * (u * FT + ct));
+                act[u] = u * FT + ct < n4;
             }
+            admit8(out, capw, wcnt, wmax, nan, v, cu, act, T, keep_pol);
         }
         g += (uint32_t)nt;
         // the warp's record of the row; the arrive releases it and the region's stores

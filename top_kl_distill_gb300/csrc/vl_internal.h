@@ -14,6 +14,7 @@ struct RowParams {
     void* x;                  // logits (fp32 or bf16, as dtype), column 0 of row 0
     int dtype;
     long long ld, ntok, V, col0, ncols;
+    long long rbeg, rend;     // rows this launch walks (a launch may take part of [0, ntok))
     const uint32_t* labels;   // CE ops; KL fold (nullable)
     const uint32_t* tid;      // KL teacher ids [ntok][k]
     const float* tp;          // KL teacher probabilities [ntok][k]
