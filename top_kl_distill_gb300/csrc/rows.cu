@@ -647,21 +647,28 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
 
 // ---------------------------------------------------------------- self-contained consumer
 
-// A row whose pass A is done and whose pass B is still to come.
+// A row whose pass A is done and whose pass B is still to come.  Two of these are live
+// across a pass A, so the record is kept small: what can be recomputed from the row
+// index (its pointer, its tile count) is, and the flags and buffer indices share a word.
 struct Pending {
     long long r;
-    void* rowp;
-    Part pt;
-    int nt;
-    bool inwin, bad;
+    int b0, bn;      // this CTA's body columns of the row (slice coordinates)
     int jl;          // slice-relative label column, -1 when none or outside this CTA's columns
+    int jht;         // this thread's head or tail column, -1 when none
     float m, lnS;
-    bool has_ht;
-    int jht;
-    float ht;
-    uint32_t xb, xpar;   // cluster exchange buffer of its statistics and the phase to wait for
-    uint32_t ab, apar;   // CE: buffer of the warps' pass A partials and the phase to wait for
-    bool first;          // this part holds column 0 of the row: it writes lse, stats, out-of-window loss
+    float ht;        // the logit at jht
+    // bit 0 in the window, bit 1 bad label, bit 2 this part holds column 0 of the row (it
+    // writes lse, stats and the out-of-window loss); bits 8-9 the cluster exchange buffer of
+    // the row's statistics and bit 10 the phase to wait for; bits 16-19 the buffer of the
+    // warps' pass A partials (CE) and bit 20 its phase
+    uint32_t f;
+    __device__ __forceinline__ bool inwin() const { return f & 1u; }
+    __device__ __forceinline__ bool bad() const { return f & 2u; }
+    __device__ __forceinline__ bool first() const { return f & 4u; }
+    __device__ __forceinline__ uint32_t xb() const { return (f >> 8) & 3u; }
+    __device__ __forceinline__ uint32_t xpar() const { return (f >> 10) & 1u; }
+    __device__ __forceinline__ uint32_t ab() const { return (f >> 16) & 15u; }
+    __device__ __forceinline__ uint32_t apar() const { return (f >> 20) & 1u; }
 };
 
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
@@ -669,19 +676,20 @@ struct Pending {
 template <typename T, int OP>
 __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane) {
     constexpr int NV = Elem<T>::NV;
-    T* const rowp = static_cast<T*>(w.rowp);
+    T* const rowp = row_ptr<T>(P, w.r);
+    const int nt = (w.bn + kTileE<T> - 1) / kTileE<T>;
     // the CE loss: the fused CE output, or beside the KL when labels come with it
     float* const ce_out = OP == kCeFused ? P.loss : OP == kKl ? P.ce_loss : nullptr;
-    const float c1 = w.inwin ? P.cg : 0.f;
+    const float c1 = w.inwin() ? P.cg : 0.f;
     const bool fold = c1 >= 0.f;
     // the gradient lines are done with: written back first, ahead of the logits that
     // pass B of the next row still re-reads from L2
     const uint64_t pol = l2_evict_first();
     const float K = fold ? w.lnS * kLog2e - log2f(c1) : 0.f;
-    for (int t = 0; t < w.nt; ++t) {
+    for (int t = 0; t < nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
-        const int n16 = min(kTileE<T>, w.pt.bn - t * kTileE<T>) / NV;
+        const int n16 = min(kTileE<T>, w.bn - t * kTileE<T>) / NV;
         uint4 raw[kVec];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
@@ -694,11 +702,11 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
         for (int u = 0; u < kVec; ++u) {
             const int j = u * NCT + ct;
             if (j < n16) {
-                const int c0 = w.pt.b0 + t * kTileE<T> + NV * j;
+                const int c0 = w.b0 + t * kTileE<T> + NV * j;
                 float x[NV], o[NV];
                 Elem<T>::unpack(raw[u], x);
                 grad_chunk<NV>(x, o, fold, w.m, w.lnS, K, c1);
-                if (w.inwin) {
+                if (w.inwin()) {
                     const unsigned d = (unsigned)(w.jl - c0);
                     if (d < (unsigned)NV) {
 #pragma unroll
@@ -713,25 +721,25 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
             }
         }
     }
-    g += (uint32_t)w.nt;
-    if (w.has_ht) {
+    g += (uint32_t)nt;
+    if (w.jht >= 0) {
         float o = c1 * soft(w.ht, w.m, w.lnS);
-        if (w.inwin && w.jht == w.jl) {
+        if (w.inwin() && w.jht == w.jl) {
             o -= P.ce_coef;
             if (ce_out) ce_out[w.r] = (w.m - w.ht) + w.lnS;
         }
         Elem<T>::put(rowp + w.jht, o);
     }
-    if (ce_out && w.first && ct == LT) {
-        if (!w.inwin) ce_out[w.r] = 0.f;
-        else if (w.bad) ce_out[w.r] = __int_as_float(0x7fc00000);
+    if (ce_out && w.first() && ct == LT) {
+        if (!w.inwin()) ce_out[w.r] = 0.f;
+        else if (w.bad()) ce_out[w.r] = __int_as_float(0x7fc00000);
     }
 }
 
 // Self-contained CE, one CTA per row: the row's statistics from the warps' partials.
 __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w, int ct) {
-    wait_parity<false>(&S.abar[w.ab], w.apar, &S.abort, &g_watchdog, P.wait_limit);
-    const MaxSum tot = combine(S.wpart[w.ab], NCW);
+    wait_parity<false>(&S.abar[w.ab()], w.apar(), &S.abort, &g_watchdog, P.wait_limit);
+    const MaxSum tot = combine(S.wpart[w.ab()], NCW);
     w.m = tot.m;
     w.lnS = logf(tot.s);
     if (ct == LT) {
@@ -744,8 +752,8 @@ __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w,
 // after its pass A.  Every rank combines the parts in rank order: the same bits.
 template <int OP>
 __device__ __forceinline__ void settle(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
-    wait_parity<true>(&S.xbar[w.xb], w.xpar, &S.abort, &g_watchdog, P.wait_limit);
-    const Part4 tot = combine4(S.xbuf[w.xb], P.csize);
+    wait_parity<true>(&S.xbar[w.xb()], w.xpar(), &S.abort, &g_watchdog, P.wait_limit);
+    const Part4 tot = combine4(S.xbuf[w.xb()], P.csize);
     w.m = tot.ms.m;
     w.lnS = logf(tot.ms.s);
     if (rank == 0 && ct == LT) {
@@ -833,21 +841,20 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         const uint32_t sb = li % kSupBufs;
         Pending cur;
         cur.r = r;
-        cur.rowp = rowp;
-        cur.pt = pt;
-        cur.nt = (pt.bn + kTileE<T> - 1) / kTileE<T>;
-        cur.inwin = inwin;
-        cur.first = rank == 0;
+        cur.b0 = pt.b0;
+        cur.bn = pt.bn;
+        const int nt = (pt.bn + kTileE<T> - 1) / kTileE<T>;
         cur.jl = -1;
-        cur.bad = false;
+        bool bad = false;
         if (has_label) {
-            if ((long long)lab_r >= P.V) cur.bad = true;
+            if ((long long)lab_r >= P.V) bad = true;
             else {
                 const long long j = (long long)lab_r - P.col0;
                 if (j >= pt.lo && j < pt.hi) cur.jl = (int)j;
             }
         }
-        if (cur.bad && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
+        cur.f = (inwin ? 1u : 0u) | (bad ? 2u : 0u) | (rank == 0 ? 4u : 0u);
+        if (bad && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
         // teacher support entries q = ct + i * NCT: column and probability to shared
         // memory for the scatter, the logit gathered now -- nothing of the row is
         // written before the barrier that ends its pass A -- for the loss
@@ -881,14 +888,14 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                 }
             }
         }
-        cur.has_ht = has_ht<T>(pt, ct);
-        cur.jht = ht_col<T>(pt, ct);
-        cur.ht = cur.has_ht ? Elem<T>::get(rowp + cur.jht) : 0.f;
+        const bool ht_here = has_ht<T>(pt, ct);
+        cur.jht = ht_here ? ht_col<T>(pt, ct) : -1;
+        cur.ht = ht_here ? Elem<T>::get(rowp + cur.jht) : 0.f;
 
         // ---- pass A: (max, sum) online over the streamed tiles
         MaxSum ms = ms_empty();
-        if (cur.has_ht) ms_add(ms, cur.ht);
-        for (int t = 0; t < cur.nt; ++t) {
+        if (ht_here) ms_add(ms, cur.ht);
+        for (int t = 0; t < nt; ++t) {
             const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
             wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
             const int n16 = min(kTileE<T>, pt.bn - t * kTileE<T>) / NV;
@@ -899,18 +906,17 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             if (lane == 0) mbar_arrive(&S.empty[slot]);
             ms_addv<NV>(ms, v);
         }
-        g += (uint32_t)cur.nt;
+        g += (uint32_t)nt;
         ms = ms_warp_reduce(ms);
         if (nobar) {
             // CE: publish this warp's partial and move on; the row's statistics are
             // collected just before its pass B, one row later, when every warp has long
             // arrived -- no CTA-wide barrier per row
-            cur.ab = nred % kPartBufs;
-            cur.apar = (nred / kPartBufs) & 1u;
+            cur.f |= ((nred % kPartBufs) << 16) | (((nred / kPartBufs) & 1u) << 20);
             ++nred;
             if (lane == 0) {
-                S.wpart[cur.ab][cw] = make_float2(ms.m, ms.s);
-                mbar_arrive(&S.abar[cur.ab]);
+                S.wpart[cur.ab()][cw] = make_float2(ms.m, ms.s);
+                mbar_arrive(&S.abar[cur.ab()]);
             }
             if (pend.r >= 0) {
                 collect(P, S, pend, ct);
@@ -948,15 +954,14 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             // row's pass B, one row later, so the exchange overlaps the next pass A.  Four
             // buffers: a peer writes buffer i + 4 only after its own collection of row
             // i + 2, which needs this CTA's part of row i + 2, sent after row i was read.
-            cur.xb = nx & 3u;
-            cur.xpar = (nx >> 2) & 1u;
+            cur.f |= ((nx & 3u) << 8) | (((nx >> 2) & 1u) << 10);
             ++nx;
             if (ct == 0) {
-                mbar_arrive_expect_tx(&S.xbar[cur.xb], 16u * (uint32_t)c);
+                mbar_arrive_expect_tx(&S.xbar[cur.xb()], 16u * (uint32_t)c);
                 const float4 mine = make_float4(tot.ms.m, tot.ms.s, tot.a, tot.b);
                 for (int q = 0; q < c; ++q)
-                    st_async_f32x4(map_to_rank(&S.xbuf[cur.xb][rank], (uint32_t)q), mine,
-                                   map_to_rank(&S.xbar[cur.xb], (uint32_t)q));
+                    st_async_f32x4(map_to_rank(&S.xbuf[cur.xb()][rank], (uint32_t)q), mine,
+                                   map_to_rank(&S.xbar[cur.xb()], (uint32_t)q));
             }
         } else {
             cur.m = tot.ms.m;
@@ -972,7 +977,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         // bf16: the label column of this row (slice coordinates; -1 none) for its rewrite
         if (kKL && sizeof(T) == 2 && ct == LT) {
             int jfull = -1;
-            if (has_label && !cur.bad) {
+            if (has_label && !bad) {
                 const long long j = (long long)lab_r - P.col0;
                 if (j >= 0 && j < ncols) jfull = (int)j;
             }

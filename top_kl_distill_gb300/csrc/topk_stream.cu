@@ -167,46 +167,52 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     return d;
 }
 
+// Value q of e[8] for a lane-varying q: a three-level select tree.
+__device__ __forceinline__ float pick8(const float (&e)[8], uint32_t q) {
+    const bool b0 = q & 1u, b1 = q & 2u, b2 = q & 4u;
+    const float t0 = b0 ? e[1] : e[0], t1 = b0 ? e[3] : e[2], t2 = b0 ? e[5] : e[4], t3 = b0 ? e[7] : e[6];
+    const float u0 = b1 ? t1 : t0, u1 = b1 ? t3 : t2;
+    return b2 ? u1 : u0;
+}
+
 // Admit this lane's 8 values of a tile (float4 u at columns cu[u] .. cu[u] + 3) that reach T
-// to the warp's region, all lanes at once: the lane's count c (0..8) in four bit planes, one
-// ballot per plane gives every lane its slot offset (the lanes below it) and the warp's
-// total; then each lane stores its values in column order.  A lane whose slots would pass
-// capw stores nothing (the warp's count passes capw: the row goes to the exact kernel).
+// to the warp's region, all lanes at once: the lane's keep mask and count c (0..8), one
+// ballot per bit plane of c gives every lane its slot offset (the lanes below it), redux the
+// warp's total; then each lane stores its kept values in column order, one loop iteration
+// per kept value (the warp runs as many as its busiest lane: one or two at a few percent
+// admitted).  A lane whose slots would pass capw stores nothing (the warp's count passes
+// capw: the row goes to the exact kernel).
 __device__ __forceinline__ void admit8(uint2* out, uint32_t capw, uint32_t& wcnt, float& wmax, bool& nan,
                                        const float4 (&v)[FVEC], const uint32_t (&cu)[FVEC], const bool (&act)[FVEC],
                                        float T, uint64_t pol) {
     static_assert(FVEC == 2, "8 values a lane: four bit planes");
     const float e[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-    bool k[8];
-    uint32_t c = 0;
+    uint32_t km = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        k[q] = act[q >> 2] && e[q] >= T;        // slots past the row's body hold -inf, which T = -inf admits
-        c += k[q] ? 1u : 0u;
-    }
+    for (int q = 0; q < 8; ++q)
+        if (act[q >> 2] && e[q] >= T) km |= 1u << q;   // slots past the row's body hold -inf, which T = -inf admits
     float mx = e[0];
 #pragma unroll
     for (int q = 1; q < 8; ++q) mx = max_nan(mx, e[q]);
     nan |= mx != mx;
-    if (!__any_sync(0xffffffffu, c != 0)) return;
+    if (!__any_sync(0xffffffffu, km != 0)) return;
+    const uint32_t c = (uint32_t)__popc(km);
     const uint32_t lt = lanemask_lt();
     const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u);
     const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
-    uint32_t pos = wcnt + (uint32_t)__popc(b0 & lt) + ((uint32_t)__popc(b1 & lt) << 1) +
-                   ((uint32_t)__popc(b2 & lt) << 2) + ((uint32_t)__popc(b3 & lt) << 3);
+    const uint32_t pos = wcnt + (uint32_t)__popc(b0 & lt) + ((uint32_t)__popc(b1 & lt) << 1) +
+                         ((uint32_t)__popc(b2 & lt) << 2) + ((uint32_t)__popc(b3 & lt) << 3);
     wcnt += __reduce_add_sync(0xffffffffu, c);
-    if (c != 0) wmax = fmaxf(wmax, mx);          // mx is NaN only with a NaN here; fmaxf skips it
-    if (c != 0 && pos + c <= capw) {
-        uint2* o = out + pos;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (k[q]) {
-                asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;"
-                             :: "l"(o), "r"(__float_as_uint(e[q])), "r"(cu[q >> 2] + (uint32_t)(q & 3)), "l"(pol)
-                             : "memory");
-                ++o;
-            }
-        }
+    if (km != 0) wmax = fmaxf(wmax, mx);          // mx is NaN only with a NaN here; fmaxf skips it
+    if (pos + c > capw) km = 0;
+    uint2* o = out + pos;
+    while (km) {
+        const uint32_t q = (uint32_t)(__ffs(km) - 1);
+        km &= km - 1u;
+        const uint32_t col = (q & 4u ? cu[1] : cu[0]) + (q & 3u);
+        asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;"
+                     :: "l"(o), "r"(__float_as_uint(pick8(e, q))), "r"(col), "l"(pol) : "memory");
+        ++o;
     }
 }
 
