@@ -548,17 +548,17 @@ def soak(torch, case, flush, until):
     return n
 
 
-def e2e_ce(torch, case, steps, warmup, chunks=8):
+def e2e_ce(torch, case, steps, warmup, chunks=4, streams=2, staged=False):
     """The headline step end to end from pinned host buffers through the C ABI.
 
-    The batch goes in row chunks through a three-stage pipeline on three streams, so that
-    the upload of chunk i + 1, the fused call on chunk i and the download of chunk i - 1
-    overlap: the copy-in stream uploads each chunk's logits and labels; the compute stream
-    waits for them and runs vl_ce_fused over the chunk's rows (the window clipped to them,
-    the batch's scale); the copy-out stream waits for that and downloads the chunk's
-    gradient, loss and lse.  Then vl_window_mean over the whole window and D2H of the
-    mean.  All of it is inside the timed region.  Returns (ms per step, H2D bytes, D2H
-    bytes, whether the host gradient equals a device-only step's)."""
+    The batch goes in row chunks so that uploads, fused calls and downloads of different
+    chunks overlap.  Per chunk: H2D of its logits and labels, vl_ce_fused over its rows
+    (the window clipped to them, the batch's scale), D2H of its gradient, loss and lse.
+    Chunks take turns on `streams` streams, each doing all three for its chunk; with
+    `staged`, one copy-in, one compute and one copy-out stream instead, linked by events.
+    Then vl_window_mean over the whole window and D2H of the mean.  All of it is inside
+    the timed region.  Returns (ms per step, H2D bytes, D2H bytes, whether the host
+    gradient equals a device-only step's)."""
     w, vl = case.w, case.vl
     n, V = w.ntok, w.V
     hx = torch.from_numpy(case.x_host).pin_memory()
@@ -568,33 +568,48 @@ def e2e_ce(torch, case, steps, warmup, chunks=8):
     hlse = torch.empty(n).pin_memory()
     hmean = torch.empty(1).pin_memory()
     x, lab = case.bufs[0], case.labels
-    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    pool = [torch.cuda.Stream() for _ in range(3 if staged else streams)]
     spans = [(i * n // chunks, (i + 1) * n // chunks) for i in range(chunks)]
     main = torch.cuda.current_stream()
 
+    def upload(r0, r1):
+        x[r0:r1].copy_(hx[r0:r1], non_blocking=True)
+        lab[r0:r1].copy_(hl[r0:r1], non_blocking=True)
+
+    def compute(r0, r1, st):
+        ls = min(max(w.loss_start - r0, 0), r1 - r0)
+        le = min(max(w.loss_end - r0, 0), r1 - r0)
+        vl.vl_ce_fused(x[r0:r1], V, r1 - r0, V, lab[r0:r1], ls, le, w.scale, case.loss[r0:r1],
+                       case.lse[r0:r1], None, None, None, st)
+
+    def download(r0, r1):
+        hg[r0:r1].copy_(x[r0:r1], non_blocking=True)
+        hloss[r0:r1].copy_(case.loss[r0:r1], non_blocking=True)
+        hlse[r0:r1].copy_(case.lse[r0:r1], non_blocking=True)
+
     def one():
         start = main.record_event()
-        s_in.wait_event(start)
-        s_run.wait_event(start)
-        s_out.wait_event(start)
-        for r0, r1 in spans:
-            with torch.cuda.stream(s_in):
-                x[r0:r1].copy_(hx[r0:r1], non_blocking=True)
-                lab[r0:r1].copy_(hl[r0:r1], non_blocking=True)
-                landed = s_in.record_event()
-            s_run.wait_event(landed)
-            ls = min(max(w.loss_start - r0, 0), r1 - r0)
-            le = min(max(w.loss_end - r0, 0), r1 - r0)
-            vl.vl_ce_fused(x[r0:r1], V, r1 - r0, V, lab[r0:r1], ls, le, w.scale, case.loss[r0:r1],
-                           case.lse[r0:r1], None, None, None, s_run)
-            done = s_run.record_event()
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                hg[r0:r1].copy_(x[r0:r1], non_blocking=True)
-                hloss[r0:r1].copy_(case.loss[r0:r1], non_blocking=True)
-                hlse[r0:r1].copy_(case.lse[r0:r1], non_blocking=True)
-        main.wait_stream(s_run)
-        main.wait_stream(s_out)
+        for st in pool:
+            st.wait_event(start)
+        if staged:
+            s_in, s_run, s_out = pool
+            for r0, r1 in spans:
+                with torch.cuda.stream(s_in):
+                    upload(r0, r1)
+                s_run.wait_event(s_in.record_event())
+                compute(r0, r1, s_run)
+                s_out.wait_event(s_run.record_event())
+                with torch.cuda.stream(s_out):
+                    download(r0, r1)
+        else:
+            for i, (r0, r1) in enumerate(spans):
+                st = pool[i % len(pool)]
+                with torch.cuda.stream(st):
+                    upload(r0, r1)
+                    compute(r0, r1, st)
+                    download(r0, r1)
+        for st in pool:
+            main.wait_stream(st)
         vl.vl_window_mean(case.loss, n, w.loss_start, w.loss_end, case.mean, main)
         hmean.copy_(case.mean, non_blocking=True)
 
@@ -926,8 +941,8 @@ def main():
     if e2e_ms is not None:
         line["e2e"] = {"value": round(case.rows() * ws / (e2e_ms * 1e-3), 1), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                       "pipeline": "8 row chunks through copy-in, compute and copy-out streams "
-                                   "(H2D, vl_ce_fused, D2H overlap); then vl_window_mean and D2H of the mean",
+                       "pipeline": "4 row chunks taking turns on 2 streams (H2D, vl_ce_fused, D2H of one "
+                                   "chunk overlap those of the others); then vl_window_mean and D2H of the mean",
                        "host_gradient_matches_device": e2e_ok}
     pool = OraclePool() if rank == 0 and not args.no_oracle else None
     if pool is not None:

@@ -43,17 +43,20 @@ constexpr int FT = FW * 32;
 constexpr int NF = 8;                       // finish warps
 constexpr int NFT = NF * 32;
 constexpr int STHREADS = 32 + FT + NFT;
-constexpr int FVEC = 2;                     // float4s of each tile per filter thread
-constexpr int FTILE = 4 * FT * FVEC;        // floats per tile (15 KB)
-constexpr int NSLOT = 10;                   // ring tiles (150 KB)
+constexpr int FVEC = 4;                     // float4s of each tile per filter thread
+constexpr int FTILE = 4 * FT * FVEC;        // floats per tile (30 KB)
+constexpr int NSLOT = 5;                    // ring tiles (150 KB)
 constexpr int NB = 2048;                    // value buckets of the finish
 constexpr int KMAX = VL_TOPK_KMAX;
 constexpr int SELCAP = KMAX + 2048;         // members of the buckets at and above the k-th's
 constexpr uint32_t FBAR = 1, NBAR = 2;      // named barriers: filter warps, finish warps
+constexpr int RT = 17;                      // finish threads per candidate region (15 x 17 = 255)
+constexpr int FB = 16;                      // candidates a finish thread loads at once
 constexpr long long kMaxStreamCols = 1LL << 20;
 
 static_assert(FTILE / 4 == FT * FVEC, "FVEC float4s of each tile per filter thread");
 static_assert(NB % NFT == 0, "buckets split evenly over the finish threads");
+static_assert(FW * RT <= NFT, "a group of finish threads per region");
 
 __device__ unsigned int g_watchdog;
 
@@ -167,41 +170,52 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     return d;
 }
 
-// Value q of e[8] for a lane-varying q: a three-level select tree.
-__device__ __forceinline__ float pick8(const float (&e)[8], uint32_t q) {
-    const bool b0 = q & 1u, b1 = q & 2u, b2 = q & 4u;
-    const float t0 = b0 ? e[1] : e[0], t1 = b0 ? e[3] : e[2], t2 = b0 ? e[5] : e[4], t3 = b0 ? e[7] : e[6];
-    const float u0 = b1 ? t1 : t0, u1 = b1 ? t3 : t2;
-    return b2 ? u1 : u0;
+// Value q of e[16] for a lane-varying q: a four-level select tree.
+__device__ __forceinline__ float pick16(const float (&e)[16], uint32_t q) {
+    const bool b0 = q & 1u, b1 = q & 2u, b2 = q & 4u, b3 = q & 8u;
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = b0 ? e[2 * i + 1] : e[2 * i];
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = b1 ? t[2 * i + 1] : t[2 * i];
+    const float w0 = b2 ? u[1] : u[0], w1 = b2 ? u[3] : u[2];
+    return b3 ? w1 : w0;
 }
 
-// Admit this lane's 8 values of a tile (float4 u at columns cu[u] .. cu[u] + 3) that reach T
-// to the warp's region, all lanes at once: the lane's keep mask and count c (0..8), one
+// Admit this lane's 16 values of a tile (float4 u at columns cu[u] .. cu[u] + 3) that reach
+// T to the warp's region, all lanes at once: the lane's keep mask and count c (0..16), one
 // ballot per bit plane of c gives every lane its slot offset (the lanes below it), redux the
 // warp's total; then each lane stores its kept values in column order, one loop iteration
-// per kept value (the warp runs as many as its busiest lane: one or two at a few percent
+// per kept value (the warp runs as many as its busiest lane: two or three at a few percent
 // admitted).  A lane whose slots would pass capw stores nothing (the warp's count passes
 // capw: the row goes to the exact kernel).
-__device__ __forceinline__ void admit8(uint2* out, uint32_t capw, uint32_t& wcnt, float& wmax, bool& nan,
-                                       const float4 (&v)[FVEC], const uint32_t (&cu)[FVEC], const bool (&act)[FVEC],
-                                       float T, uint64_t pol) {
-    static_assert(FVEC == 2, "8 values a lane: four bit planes");
-    const float e[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+__device__ __forceinline__ void admit16(uint2* out, uint32_t capw, uint32_t& wcnt, float& wmax, bool& nan,
+                                        const float4 (&v)[FVEC], const uint32_t (&cu)[FVEC], const bool (&act)[FVEC],
+                                        float T, uint64_t pol) {
+    static_assert(FVEC == 4, "16 values a lane: five bit planes");
+    float e[16];
+#pragma unroll
+    for (int u = 0; u < FVEC; ++u) {
+        e[4 * u] = v[u].x;
+        e[4 * u + 1] = v[u].y;
+        e[4 * u + 2] = v[u].z;
+        e[4 * u + 3] = v[u].w;
+    }
     uint32_t km = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < 16; ++q)
         if (act[q >> 2] && e[q] >= T) km |= 1u << q;   // slots past the row's body hold -inf, which T = -inf admits
     float mx = e[0];
 #pragma unroll
-    for (int q = 1; q < 8; ++q) mx = max_nan(mx, e[q]);
+    for (int q = 1; q < 16; ++q) mx = max_nan(mx, e[q]);
     nan |= mx != mx;
     if (!__any_sync(0xffffffffu, km != 0)) return;
     const uint32_t c = (uint32_t)__popc(km);
     const uint32_t lt = lanemask_lt();
-    const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u);
-    const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
-    const uint32_t pos = wcnt + (uint32_t)__popc(b0 & lt) + ((uint32_t)__popc(b1 & lt) << 1) +
-                         ((uint32_t)__popc(b2 & lt) << 2) + ((uint32_t)__popc(b3 & lt) << 3);
+    uint32_t pos = wcnt;
+#pragma unroll
+    for (int b = 0; b < 5; ++b) pos += (uint32_t)__popc(__ballot_sync(0xffffffffu, (c >> b) & 1u) & lt) << b;
     wcnt += __reduce_add_sync(0xffffffffu, c);
     if (km != 0) wmax = fmaxf(wmax, mx);          // mx is NaN only with a NaN here; fmaxf skips it
     if (pos + c > capw) km = 0;
@@ -209,9 +223,9 @@ __device__ __forceinline__ void admit8(uint2* out, uint32_t capw, uint32_t& wcnt
     while (km) {
         const uint32_t q = (uint32_t)(__ffs(km) - 1);
         km &= km - 1u;
-        const uint32_t col = (q & 4u ? cu[1] : cu[0]) + (q & 3u);
+        const uint32_t col = cu[0] + (q >> 2) * (uint32_t)(4 * FT) + (q & 3u);
         asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;"
-                     :: "l"(o), "r"(__float_as_uint(pick8(e, q))), "r"(col), "l"(pol) : "memory");
+                     :: "l"(o), "r"(__float_as_uint(pick16(e, q))), "r"(col), "l"(pol) : "memory");
         ++o;
     }
 }
@@ -251,7 +265,7 @@ __device__ void filter_warps(const StreamParams& F, KSmem& S) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
             if (t == 0) {
-                // the threshold from the first tile (every row here has at least 8 full tiles)
+                // the threshold from the first tile (every row here has at least 4 full tiles)
                 const float e = warp_kth<FVEC>(v, (uint32_t)F.spec_a, lane);
                 if (lane == 0) S.wspec[p][cw] = e;
                 named_sync(FBAR, FT);
@@ -278,7 +292,7 @@ __device__ void filter_warps(const StreamParams& F, KSmem& S) {
                 cu[u] = (uint32_t)(h + t * FTILE + 4 * (u * FT + ct));
                 act[u] = u * FT + ct < n4;
             }
-            admit8(out, capw, wcnt, wmax, nan, v, cu, act, T, keep_pol);
+            admit16(out, capw, wcnt, wmax, nan, v, cu, act, T, keep_pol);
         }
         g += (uint32_t)nt;
         // the warp's record of the row; the arrive releases it and the region's stores
@@ -357,13 +371,22 @@ __device__ void finish_warps(const StreamParams& F, KSmem& S) {
         const uint2* area = region(F, p);
         bool ok = hist;
         uint32_t bstar = 0, nsel = 0;
+        // each region is read by its own group of RT threads, FB candidates a thread at a time:
+        // the loads of a pass go out together, one L2 round trip while the stream loads L2
+        const int rw = ft / RT, rs = ft % RT;
+        const uint32_t rc = rw < FW ? min(S.wcnt[p][rw], capw) : 0u;
+        const uint2* rin = area + (long long)(rw < FW ? rw : 0) * capw;
         if (hist) {
-            for (int w = fw; w < FW; w += NF) {
-                const uint32_t c = min(S.wcnt[p][w], capw);
-                const uint2* in = area + (long long)w * capw;
-#pragma unroll 4
-                for (uint32_t j = (uint32_t)lane; j < c; j += 32)
-                    atomicAdd(&S.hcnt[bucket(f2key(__uint_as_float(in[j].x)))], 1u);
+            for (uint32_t j0 = (uint32_t)rs; j0 < rc; j0 += RT * FB) {
+                uint32_t x[FB];
+#pragma unroll
+                for (int i = 0; i < FB; ++i) {
+                    const uint32_t j = j0 + (uint32_t)(i * RT);
+                    if (j < rc) x[i] = rin[j].x;
+                }
+#pragma unroll
+                for (int i = 0; i < FB; ++i)
+                    if (j0 + (uint32_t)(i * RT) < rc) atomicAdd(&S.hcnt[bucket(f2key(__uint_as_float(x[i])))], 1u);
             }
             named_sync(NBAR, NFT);
             // bucket starts in descending order; thread ft owns buckets [c0, c0 + PER)
@@ -397,19 +420,23 @@ __device__ void finish_warps(const StreamParams& F, KSmem& S) {
             nsel = S.nsel;
             ok = nsel <= (uint32_t)SELCAP;
             if (ok) {
-                for (int w = fw; w < FW; w += NF) {
-                    const uint32_t c = min(S.wcnt[p][w], capw);
-                    const uint2* in = area + (long long)w * capw;
-#pragma unroll 4
-                    for (uint32_t j = (uint32_t)lane; j < c; j += 32) {
-                        const uint2 e = in[j];
-                        const uint32_t kk = f2key(__uint_as_float(e.x));
+                for (uint32_t j0 = (uint32_t)rs; j0 < rc; j0 += RT * FB) {
+                    uint2 e[FB];
+#pragma unroll
+                    for (int i = 0; i < FB; ++i) {
+                        const uint32_t j = j0 + (uint32_t)(i * RT);
+                        if (j < rc) e[i] = rin[j];
+                    }
+#pragma unroll
+                    for (int i = 0; i < FB; ++i) {
+                        if (j0 + (uint32_t)(i * RT) >= rc) continue;
+                        const uint32_t kk = f2key(__uint_as_float(e[i].x));
                         const uint32_t b = bucket(kk);
                         if (b >= bstar) {
                             const uint32_t q = atomicAdd(&S.hpos[b], 1u);
                             if (q < (uint32_t)SELCAP) {
                                 S.skey[q] = kk;
-                                S.sid[q] = e.y;
+                                S.sid[q] = e[i].y;
                             }
                         }
                     }
@@ -502,17 +529,19 @@ long long list_bytes(long long rows) { return (16 + 4 * rows + 255) / 256 * 256;
 
 }  // namespace
 
-// Rows qualify when they have at least 8 full tiles (the first one is a sample of the row),
-// at most 2^20 columns, and the warp estimates' rank stays small.  The rank a puts about
-// 1.9 k of the row's values above T on average: on the teacher workload's rows (k = 2048 of
-// 128256) the count stays within 3.4 standard deviations of its mean over 4096 rows, and
-// falling short of k is a 5-deviation event.
+// Rows qualify when they have at least 4 full tiles (the first one is a sample of the row),
+// at most 2^20 columns, and the warp estimates' rank stays small.  Each warp's estimate is
+// the a-th largest of its 512 values of the first tile, about a V / 512 values of the row
+// pass T, and the count's relative spread is about 1 / sqrt(15 a) (the mean of 15 order
+// statistics).  a is the smallest rank that keeps k at least 5.5 spreads below the mean:
+// a = 14 for k = 2048 of 128256 columns (mean 3449 admitted, standard deviation 228 over
+// the 4096 teacher rows, first tiles simulated), a = 4 for k = 256 (919 and 122).
 int topk_filter_spec_a(long long V, int k) {
-    if (V < 8LL * FTILE || V > kMaxStreamCols) return 0;
+    if (V < 4LL * FTILE || V > kMaxStreamCols) return 0;
     const double share = (double)k * (double)(FTILE / FW) / (double)V;
-    int a = (int)ceil(1.9 * share);
-    if (a < 3) a = 3;
-    return a <= FTILE / FW / 8 ? a : 0;
+    for (int a = 2; a <= FTILE / FW / 8; ++a)
+        if ((double)a * 0.97 / share * (1.0 - 5.5 / sqrt(15.0 * a)) >= 1.0) return a;
+    return 0;
 }
 
 // Slots of a warp's region: the expected admissions m = a V / (256 * 15), plus six binomial

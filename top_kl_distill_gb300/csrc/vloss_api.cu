@@ -104,13 +104,13 @@ Grid choose_grid(int op, bool resident, long long rows, long long ncols, int dty
     }
     // Self-contained mode re-reads a row part in pass B from L2 while the next part is
     // read: about two parts of esize ncols / c bytes per CTA are live.  Splitting a row over
-    // c CTAs keeps them within a third of L2 for fp32 (c = 4 at 128256 columns on a GB300).
-    // bf16 rows cost twice the arithmetic per byte, so the kernel is issue-bound before it is
-    // HBM-bound and a cluster's per-row exchange costs more than the re-reads that spill
-    // from L2: bf16 takes up to 0.6 of L2 (c = 1 at 128256 columns: 1.04 ms against 1.27 ms
-    // with c = 2 for 8192 rows on a GB300).
+    // c CTAs keeps them within 0.4 of L2 for fp32 (c = 3 at 128256 columns on a GB300: 1.46 ms
+    // for 8192 rows, against 1.51 ms with c = 4 and 1.86 ms with c = 2).  bf16 rows cost
+    // twice the arithmetic per byte, so the kernel is issue-bound before it is HBM-bound and a
+    // cluster's per-row exchange costs more than the re-reads that spill from L2: bf16 takes
+    // up to 0.6 of L2 (c = 1 at 128256 columns: 1.01 ms against 1.23 ms with c = 2).
     const double live = 2.0 * (dtype == kBf16 ? 2.0 : 4.0) * (double)ncols * (double)sms;
-    const double budget = l2_bytes() > 0 ? l2_bytes() * (dtype == kBf16 ? 0.6 : 1.0 / 3.0) : 40e6;
+    const double budget = l2_bytes() > 0 ? l2_bytes() * (dtype == kBf16 ? 0.6 : 0.4) : 40e6;
     int cmin = 1;
     while (cmin < kMaxCluster && live / cmin > budget) ++cmin;
     static const int forced = [] {
