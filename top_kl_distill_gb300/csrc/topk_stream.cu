@@ -57,6 +57,7 @@ constexpr long long kMaxStreamCols = 1LL << 20;
 static_assert(FTILE / 4 == FT * FVEC, "FVEC float4s of each tile per filter thread");
 static_assert(NB % NFT == 0, "buckets split evenly over the finish threads");
 static_assert(FW * RT <= NFT, "a group of finish threads per region");
+static_assert(KMAX % NFT == 0, "output positions split evenly over the finish threads");
 
 __device__ unsigned int g_watchdog;
 
@@ -471,20 +472,33 @@ __device__ void finish_warps(const StreamParams& F, KSmem& S) {
             for (int b = ft; b < NB; b += NFT) S.hcnt[b] = 0u;
         if (ok) {
             // probabilities renormalised over the k
+            // (each thread keeps the exponentials of its positions for the write)
+            constexpr int QPT = KMAX / NFT;
             const float v0 = key2f(S.okey[0]);
+            float ez[QPT];
             float part = 0.f;
-            for (uint32_t q = (uint32_t)ft; q < K; q += NFT) part += expf(key2f(S.okey[q]) - v0);
+#pragma unroll
+            for (int i = 0; i < QPT; ++i) {
+                const uint32_t q = (uint32_t)(ft + i * NFT);
+                ez[i] = q < K ? expf(key2f(S.okey[q]) - v0) : 0.f;
+                part += ez[i];
+            }
             part = warp_sum(part);
             if (lane == 0) S.zred[fw] = part;
             named_sync(NBAR, NFT);
             float Z = 0.f;
 #pragma unroll
             for (int w = 0; w < NF; ++w) Z += S.zred[w];
+            const float rZ = 1.0f / Z;
             uint32_t* oi = F.ids + r * (long long)K;
             float* op = F.probs + r * (long long)K;
-            for (uint32_t q = (uint32_t)ft; q < K; q += NFT) {
-                oi[q] = S.oid[q];
-                op[q] = expf(key2f(S.okey[q]) - v0) / Z;
+#pragma unroll
+            for (int i = 0; i < QPT; ++i) {
+                const uint32_t q = (uint32_t)(ft + i * NFT);
+                if (q < K) {
+                    oi[q] = S.oid[q];
+                    op[q] = ez[i] * rZ;
+                }
             }
         }
     }
