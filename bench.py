@@ -55,6 +55,57 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 TFLOP/s of a kernel timed alone (the burst figure), measured or fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def head_gemm_line(torch, flush, M=2048, N=128256, K=4096, reps=10):
+    """The vocabulary head's logits GEMM (a chunk of 2048 hidden rows of 4096 against a
+    128256 x 4096 weight plane, bf16 in, fp32 out) on the tensor-core kernel, timed alone
+    with CUDA events after an L2 flush; cuBLAS (torch.matmul, bf16 out) on the same shape
+    as context."""
+    from top_kl_distill_gb300 import vloss as vl
+    g = torch.Generator(device="cuda").manual_seed(20260)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    D = torch.empty(M, N, device="cuda")
+    Dr = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ms = []
+        for _ in range(reps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return sorted(ms)[len(ms) // 2]
+
+    ms = timed(lambda: vl.vl_gemm_bf16_tn(A, B, D, M, N, K, N, 1.0))
+    ms_ref = timed(lambda: torch.matmul(A, B.t(), out=Dr))
+    peak, kind = bf16_peak()
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    out = {"shape": f"M {M} x N {N} x K {K}, bf16 in, fp32 out", "ms": round(ms, 4),
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(tf / peak, 4), "peak_source": kind, "kernel": "tc_gemm"},
+           "cublas_bf16_out_tflops": round(2.0 * M * N * K / (ms_ref * 1e-3) / 1e12, 1), "gpu_launches": 1}
+    del A, B, D, Dr
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -955,7 +1006,7 @@ def main():
         names = ["ce_tiny", "ce_lm_bf16", "kl", "topk_k256", "topk_k2048", "large_v", "large_v_bf16",
                  "large_v_sliced"]
         if args.sweep_only:
-            names = [n for n in args.sweep_only.split(",") if n]
+            names = [n for n in args.sweep_only.split(",") if n and n != "head_gemm"]
         for name in names:
             c = make_case(torch, name, args.ntok or None, args.bufs or None)
             steps = args.sweep_steps
@@ -974,6 +1025,8 @@ def main():
             sweep[name] = entry
             del c
             torch.cuda.empty_cache()
+        if not args.sweep_only or "head_gemm" in args.sweep_only.split(","):
+            sweep["head_gemm"] = head_gemm_line(torch, flush)
         line["sweep"] = sweep
 
     if pool is not None:

@@ -103,11 +103,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap ta,
                                                         const __grid_constant__ CUtensorMap tb, float* __restrict__ D,
-                                                        long long ldd, int M, int N, int K, float alpha) {
+                                                        long long ldd, int M, int N, int K, float alpha, int m_fast) {
     extern __shared__ uint8_t gsm_raw[];
     GSmem& S = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int m0 = (m_fast ? blockIdx.x : blockIdx.y) * BM, n0 = (m_fast ? blockIdx.y : blockIdx.x) * BN;
     const int nk = (K + BK - 1) / BK;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -229,7 +229,7 @@ size_t tc_gemm_smem() { return sizeof(GSmem) + 1024; }
 // K a multiple of 8.  cudaErrorInvalidValue when the shapes do not qualify.
 cudaError_t tc_gemm_tn(const void* A, const void* B, float* D, long long M, long long N, long long K, long long ldd,
                        float alpha, cudaStream_t st) {
-    if (M < 1 || N < 1 || K < 8 || K % 8 != 0 || M > 65535LL * BM || N > (1LL << 31) - BN || K > (1LL << 31))
+    if (M < 1 || N < 1 || K < 8 || K % 8 != 0 || M > (1LL << 31) - BM || N > (1LL << 31) - BN || K > (1LL << 31))
         return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return cudaErrorInvalidValue;
     int dev = 0;
@@ -245,7 +245,15 @@ cudaError_t tc_gemm_tn(const void* A, const void* B, float* D, long long M, long
     CUtensorMap ta, tb;
     if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, BN)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), 1);
+    // Tile order: the CTAs that run together share the tiles of the larger operand, which is
+    // then read from HBM about once, while the smaller one is re-read (from L2 when it fits).
+    // M-tiles vary fastest when A is the smaller operand (the head's logits: a chunk of hidden
+    // rows against the whole weight plane), N-tiles otherwise.
+    const long long mt = (M + BM - 1) / BM, ntl = (N + BN - 1) / BN;
+    int m_fast = M <= N ? 1 : 0;
+    if ((m_fast ? ntl : mt) > 65535) m_fast ^= 1;          // the slow grid dimension holds at most 65535
+    if ((m_fast ? ntl : mt) > 65535) return cudaErrorInvalidValue;
+    cfg.gridDim = m_fast ? dim3((unsigned)mt, (unsigned)ntl, 1) : dim3((unsigned)ntl, (unsigned)mt, 1);
     cfg.blockDim = dim3(GT, 1, 1);
     cfg.dynamicSmemBytes = tc_gemm_smem();
     cfg.stream = st;
@@ -254,7 +262,7 @@ cudaError_t tc_gemm_tn(const void* A, const void* B, float* D, long long M, long
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, ta, tb, D, ldd, (int)M, (int)N, (int)K, alpha);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, ta, tb, D, ldd, (int)M, (int)N, (int)K, alpha, m_fast);
 }
 
 unsigned int gemm_watchdog(bool clear) {
