@@ -683,23 +683,32 @@ def e2e_ce(torch, case, steps, warmup, chunks=4, streams=2, staged=False):
     return ms, h2d, d2h, ok
 
 
+# The sources each measured kernel is built from: its DRAM traffic in profiles/ncu_traffic.json
+# stands only while these files are unchanged since the capture.
+ROW_SOURCES = ("rows.cu", "vl_device.cuh", "vl_internal.h", "vloss_api.cu")
+TOPK_SOURCES = ("topk_stream.cu", "topk.cu", "vl_topk.cuh", "vl_device.cuh", "vl_internal.h", "vloss_api.cu")
+KERNEL_SOURCES = {"ce_fused": ROW_SOURCES, "ce_fused_tiny": ROW_SOURCES, "ce_fused_bf16": ROW_SOURCES,
+                  "kl_resident": ROW_SOURCES, "ce_kl_fused": ROW_SOURCES, "ce_kl_fused_bf16": ROW_SOURCES,
+                  "kl_sliced_stream": ROW_SOURCES, "topk_k256": TOPK_SOURCES, "topk_k2048": TOPK_SOURCES}
+
+
 def kernel_traffic(kernel_tag: str):
-    """DRAM bytes per launch from the committed ncu summary, if the sources still match."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources still match."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kernel_tag not in KERNEL_SOURCES:
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("csrc_sha256") != csrc_hash():
-        return None
     e = d.get("kernels", {}).get(kernel_tag)
-    return None if e is None else e.get("dram_bytes_per_launch")
+    if e is None or e.get("sources_sha256") != sources_hash(KERNEL_SOURCES[kernel_tag]):
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
-def csrc_hash() -> str:
+def sources_hash(names) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "top_kl_distill_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(names):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()

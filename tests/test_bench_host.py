@@ -30,23 +30,30 @@ def test_clock_summary_median_window_and_reasons():
     assert empty["samples"] == 0 and empty["sm_mhz"] is None
 
 
-def test_traffic_table_follows_the_sources(tmp_path, monkeypatch):
+def test_traffic_table_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """A kernel's DRAM bytes count only while its own sources are unchanged since the capture."""
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "ncu_traffic.json").write_text(json.dumps(
-        {"csrc_sha256": bench.csrc_hash(), "kernels": {"ce_fused": {"dram_bytes_per_launch": 123}}}))
-    real_hash = bench.csrc_hash()
+    csrc = tmp_path / "top_kl_distill_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in set(bench.ROW_SOURCES) | set(bench.TOPK_SOURCES):
+        (csrc / f).write_text(f"// {f}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "csrc_hash", lambda: real_hash)
+    row_hash = bench.sources_hash(bench.ROW_SOURCES)
+    (prof / "ncu_traffic.json").write_text(json.dumps(
+        {"kernels": {"ce_fused": {"dram_bytes_per_launch": 123, "sources_sha256": row_hash},
+                     "topk_k256": {"dram_bytes_per_launch": 456, "sources_sha256": "0" * 64}}}))
     assert bench.kernel_traffic("ce_fused") == 123
+    assert bench.kernel_traffic("topk_k256") is None           # captured from other sources
     assert bench.kernel_traffic("no_such_kernel") is None
-    monkeypatch.setattr(bench, "csrc_hash", lambda: "0" * 64)      # the kernels changed since the capture
+    (csrc / "rows.cu").write_text("// changed\n")               # the row kernels changed since the capture
     assert bench.kernel_traffic("ce_fused") is None
 
 
-def test_csrc_hash_is_stable_and_source_sensitive():
-    assert bench.csrc_hash() == bench.csrc_hash()
-    assert len(bench.csrc_hash()) == 64
+def test_sources_hash_is_stable_and_source_sensitive():
+    assert bench.sources_hash(bench.ROW_SOURCES) == bench.sources_hash(bench.ROW_SOURCES)
+    assert len(bench.sources_hash(bench.ROW_SOURCES)) == 64
+    assert bench.sources_hash(bench.ROW_SOURCES) != bench.sources_hash(bench.TOPK_SOURCES)
 
 
 def test_roofline_arithmetic():
