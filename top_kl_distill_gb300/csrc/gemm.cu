@@ -3,18 +3,24 @@
 // Used for the vocabulary head around the losses (cortiq-engine train_head.rs: mm_cols for the
 // logits, hidden . W^T; and the backward mm over the transposed weight plane wt, dlogits . wt^T).
 //
-// One CTA computes one 128 x 256 tile of D:
+// One persistent CTA per SM walks 128 x 256 tiles of D (blockIdx.x, blockIdx.x + gridDim.x, ...):
 //   warp 0    TMA producer: 2-D tiled bulk copies of 128 x 64 (A) and 256 x 64 (B) bf16 boxes
-//             with 128-byte swizzle into a 4-stage shared-memory ring, signalled on mbarriers;
-//   warp 1    allocates 256 columns of tensor memory and, from one thread, issues
-//             tcgen05.mma (kind::f16, M = 128, N = 256, K = 16; four per 64-wide stage), then
-//             tcgen05.commit to the stage's empty barrier (the stage is free once its MMAs
-//             have read it) and, after the last stage, to the accumulator barrier;
-//   warps 2-5 the epilogue: tcgen05.ld of their 32-lane quarter of the accumulator (row i of
-//             the tile is tensor-memory lane i, column j is column j), alpha, stores to D.
+//             with 128-byte swizzle into a 4-stage shared-memory ring, signalled on mbarriers,
+//             the ring's position running on across tiles;
+//   warp 1    allocates 512 columns of tensor memory (two 128 x 256 fp32 accumulators) and,
+//             from one thread, issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16; four per
+//             64-wide stage) into the accumulator of the tile's parity, once the epilogue has
+//             handed it back; tcgen05.commit to the stage's empty barrier (the stage is free once
+//             its MMAs have read it) and, after the tile's last stage, to the accumulator's full
+//             barrier;
+//   warps 2-5 the epilogue: tcgen05.ld of their 32-lane quarter of a full accumulator (row i of
+//             the tile is tensor-memory lane i, column j is column j), alpha, stores to D, then
+//             an arrival that hands the accumulator back -- so the stores of tile i overlap the
+//             MMAs of tile i + 1.
 // Rows, columns and K past the matrix edges: the TMA fills zeros, the epilogue masks stores.
 // Every wait is bounded; a wait that runs out raises the watchdog word, the producer still
-// waits for its copies in flight, and tensor memory is always freed before the CTA exits.
+// waits for its copies in flight, and tensor memory is freed only after a final commit shows
+// every MMA issued complete.
 #include "vl_device.cuh"
 #include "vl_internal.h"
 
@@ -31,7 +37,7 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB: 128 rows of 128 bytes
 constexpr int B_BYTES = BN * BK * 2;        // 32 KB
 constexpr int GT = 192;                     // six warps
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 2 * BN;          // two accumulators of 128 x 256 fp32
 
 __device__ unsigned int g_watchdog;
 
@@ -40,7 +46,9 @@ struct alignas(1024) GSmem {
     uint8_t b[STAGES][B_BYTES];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t accum;
+    uint64_t tfull[2];                      // an accumulator's tile is complete (MMA commit)
+    uint64_t tempty[2];                     // the epilogue has read an accumulator
+    uint64_t done;                          // every MMA issued has completed
     uint32_t tmem_base;
     int abort;
 };
@@ -107,14 +115,25 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     extern __shared__ uint8_t gsm_raw[];
     GSmem& S = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = (m_fast ? blockIdx.x : blockIdx.y) * BM, n0 = (m_fast ? blockIdx.y : blockIdx.x) * BN;
+    const int mt = (M + BM - 1) / BM, ntl = (N + BN - 1) / BN;
+    const int tiles = mt * ntl;
     const int nk = (K + BK - 1) / BK;
+    // tile t of this CTA's sequence blockIdx.x, blockIdx.x + gridDim.x, ...: its (m0, n0)
+    auto tile_at = [&](int t, int& m0, int& n0) {
+        const int a = m_fast ? t % mt : t / ntl, b = m_fast ? t / mt : t % ntl;
+        m0 = a * BM;
+        n0 = b * BN;
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
         }
-        mbar_init(&S.accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.tfull[b], 1);
+            mbar_init(&S.tempty[b], 4);      // one arrival per epilogue warp
+        }
+        mbar_init(&S.done, 1);
         S.abort = 0;
         fence_mbar_init_cluster();
     }
@@ -132,63 +151,94 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES, use = kb / STAGES;
-                if (use > 0 && !wait_parity<false>(&S.empty[s], (use - 1) & 1u, &S.abort, &g_watchdog)) break;
-                mbar_arrive_expect_tx(&S.full[s], A_BYTES + B_BYTES);
-                tma_load_2d(S.a[s], &ta, kb * BK, m0, &S.full[s]);
-                tma_load_2d(S.b[s], &tb, kb * BK, n0, &S.full[s]);
-                ++issued;
+            uint32_t g = 0, issued = 0;
+            bool stop = false;
+            for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+                int m0, n0;
+                tile_at(t, m0, n0);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t s = g % STAGES, use = g / STAGES;
+                    if (use > 0 && !wait_parity<false>(&S.empty[s], (use - 1) & 1u, &S.abort, &g_watchdog)) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&S.full[s], A_BYTES + B_BYTES);
+                    tma_load_2d(S.a[s], &ta, kb * BK, m0, &S.full[s]);
+                    tma_load_2d(S.b[s], &tb, kb * BK, n0, &S.full[s]);
+                    issued = g + 1;
+                }
             }
             // every copy issued has landed before the CTA can leave
-            for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-                wait_parity_drain(&S.full[kb % STAGES], (kb / STAGES) & 1u);
+            for (uint32_t gg = issued > (uint32_t)STAGES ? issued - STAGES : 0u; gg < issued; ++gg)
+                wait_parity_drain(&S.full[gg % STAGES], (gg / STAGES) & 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES;
-                if (!wait_parity<false>(&S.full[s], (kb / STAGES) & 1u, &S.abort, &g_watchdog)) break;
+            uint32_t g = 0, i = 0;
+            bool stop = false;
+            for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x, ++i) {
+                const uint32_t b = i & 1u, use = i >> 1;
+                // the epilogue has read this accumulator's previous tile
+                if (use > 0 && !wait_parity<false>(&S.tempty[b], (use - 1) & 1u, &S.abort, &g_watchdog)) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
+                const uint32_t acc = tmem + b * (uint32_t)BN;
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t s = g % STAGES;
+                    if (!wait_parity<false>(&S.full[s], (g / STAGES) & 1u, &S.abort, &g_watchdog)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    mma_bf16(tmem, sw128_desc(a0 + 32u * k), sw128_desc(b0 + 32u * k), (kb | k) != 0 ? 1u : 0u);
-                mma_commit(&S.empty[s]);        // the stage is free once these MMAs have read it
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16(acc, sw128_desc(a0 + 32u * k), sw128_desc(b0 + 32u * k), (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&S.empty[s]);        // the stage is free once these MMAs have read it
+                }
+                if (!stop) mma_commit(&S.tfull[b]); // the tile's accumulator is complete
             }
-            mma_commit(&S.accum);               // always: the epilogue and the dealloc wait for it
+            mma_commit(&S.done);                    // always: the dealloc waits for every MMA issued
         }
         __syncwarp();
     } else {
-        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 of the tile's accumulator
         const int q = warp & 3;
-        const bool ok = wait_parity<false>(&S.accum, 0u, &S.abort, &g_watchdog);
-        tc_fence_after();
-        const int row = m0 + 32 * q + lane;
         const bool vec = (ldd & 3) == 0 && (reinterpret_cast<uintptr_t>(D) & 15u) == 0;
-        for (int c = 0; c < BN; c += 32) {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c, v);
-            if (!ok || row >= M) continue;
-            float* out = D + (long long)row * ldd + n0 + c;
-            if (vec && n0 + c + 32 <= N) {
+        uint32_t i = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const uint32_t b = i & 1u;
+            if (!wait_parity<false>(&S.tfull[b], (i >> 1) & 1u, &S.abort, &g_watchdog)) break;
+            tc_fence_after();
+            int m0, n0;
+            tile_at(t, m0, n0);
+            const int row = m0 + 32 * q + lane;
+            for (int c = 0; c < BN; c += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + b * (uint32_t)BN + (uint32_t)c, v);
+                if (row >= M) continue;
+                float* out = D + (long long)row * ldd + n0 + c;
+                if (vec && n0 + c + 32 <= N) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(out + j) =
-                        make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
-            } else {
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(out + j) =
+                            make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (n0 + c + j < N) out[j] = alpha * v[j];
+                    for (int j = 0; j < 32; ++j)
+                        if (n0 + c + j < N) out[j] = alpha * v[j];
+                }
             }
+            // this warp's reads of the accumulator are done (tcgen05.ld waited): hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.tempty[b]);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        // the MMAs are done writing before their columns are freed (at once, unless a wait ran out)
-        wait_parity_drain(&S.accum, 0u);
+        // every MMA issued has completed before the columns are freed
+        wait_parity_drain(&S.done, 0u);
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
     }
@@ -244,16 +294,23 @@ cudaError_t tc_gemm_tn(const void* A, const void* B, float* D, long long M, long
     }
     CUtensorMap ta, tb;
     if (!make_map(&ta, A, M, K, BM) || !make_map(&tb, B, N, K, BN)) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
     // Tile order: the CTAs that run together share the tiles of the larger operand, which is
     // then read from HBM about once, while the smaller one is re-read (from L2 when it fits).
     // M-tiles vary fastest when A is the smaller operand (the head's logits: a chunk of hidden
-    // rows against the whole weight plane), N-tiles otherwise.
+    // rows against the whole weight plane), N-tiles otherwise.  One persistent CTA per SM
+    // walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... of that order.
     const long long mt = (M + BM - 1) / BM, ntl = (N + BN - 1) / BN;
-    int m_fast = M <= N ? 1 : 0;
-    if ((m_fast ? ntl : mt) > 65535) m_fast ^= 1;          // the slow grid dimension holds at most 65535
-    if ((m_fast ? ntl : mt) > 65535) return cudaErrorInvalidValue;
-    cfg.gridDim = m_fast ? dim3((unsigned)mt, (unsigned)ntl, 1) : dim3((unsigned)ntl, (unsigned)mt, 1);
+    if (mt * ntl > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int m_fast = M <= N ? 1 : 0;
+    static std::atomic<int> sm_cache[64];
+    int sms = sm_cache[dev].load(std::memory_order_acquire);
+    if (sms <= 0) {
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        sm_cache[dev].store(sms, std::memory_order_release);
+    }
+    const long long tiles = mt * ntl;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms), 1, 1);
     cfg.blockDim = dim3(GT, 1, 1);
     cfg.dynamicSmemBytes = tc_gemm_smem();
     cfg.stream = st;
