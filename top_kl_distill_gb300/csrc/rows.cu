@@ -163,6 +163,10 @@ struct alignas(128) Smem {
             float kp[2][KMAX];               // probability per entry
             float ks[2][KMAX];               // the logit at that column, gathered as its tile passes
         };
+        struct {                        // self-contained CE over a cluster: every warp's pass A partial of
+                                        // the row's parts, from every rank (4 rows in flight)
+            float2 xw[4][kMaxCluster][NCW];
+        };
         struct {                        // self-contained mode: support of the last kSupBufs rows
             alignas(16) int ecol[kSupBufs][KSELF];   // support column (slice-relative; -1 elsewhere)
             float ep[kSupBufs][KSELF];
@@ -748,6 +752,20 @@ __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w,
     }
 }
 
+// Self-contained CE over a cluster: the row's statistics from every warp of every rank,
+// sent with st.async after each warp's pass A; every rank combines them in the same order
+// (rank, then warp), so all hold the same bits.
+__device__ __forceinline__ void collect_cluster(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
+    wait_parity<true>(&S.xbar[w.xb()], w.xpar(), &S.abort, &g_watchdog, P.wait_limit);
+    const MaxSum tot = combine(&S.xw[w.xb()][0][0], P.csize * NCW);
+    w.m = tot.m;
+    w.lnS = logf(tot.s);
+    if (rank == 0 && ct == LT) {
+        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
+        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
+    }
+}
+
 // Cluster mode: the row's statistics (and KL loss parts) from every rank's part, sent
 // after its pass A.  Every rank combines the parts in rank order: the same bits.
 template <int OP>
@@ -809,7 +827,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const int ncols = (int)P.ncols;
     const bool has_label = (OP != kKl) || P.labels != nullptr;
     // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
-    const bool nobar = !kKL && c == 1 && ncols >= 2 * NV;
+    const bool nobar = !kKL && ncols >= 2 * NV * c;
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
     long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (support scatter owed)
     uint32_t nlab = 0, nid = 0;
@@ -908,6 +926,28 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         }
         g += (uint32_t)nt;
         ms = ms_warp_reduce(ms);
+        if (nobar && c > 1) {
+            // CE over a cluster: this warp's partial goes to every rank (st.async completing the
+            // rank's exchange barrier, whose one local arrival carries the bytes expected); the
+            // row is collected just before its pass B, one row later -- no CTA barrier per row.
+            // Four buffers: a warp writes buffer i + 4 only after its own collection of row
+            // i + 2, which needs every warp's partial of row i + 2, each sent after that warp's
+            // collection of row i.
+            cur.f |= ((nx & 3u) << 8) | (((nx >> 2) & 1u) << 10);
+            ++nx;
+            if (ct == 0) mbar_arrive_expect_tx(&S.xbar[cur.xb()], 8u * (uint32_t)(c * NCW));
+            if (lane == 0)
+                for (int q = 0; q < c; ++q)
+                    st_async_f32x2(map_to_rank(&S.xw[cur.xb()][rank][cw], (uint32_t)q), ms.m, ms.s,
+                                   map_to_rank(&S.xbar[cur.xb()], (uint32_t)q));
+            if (pend.r >= 0) {
+                collect_cluster(P, S, pend, ct, rank);
+                pass_b<T, OP>(P, S, pend, g, ct, lane);
+            }
+            pend = cur;
+            ++li;
+            continue;
+        }
         if (nobar) {
             // CE: publish this warp's partial and move on; the row's statistics are
             // collected just before its pass B, one row later, when every warp has long
@@ -1000,7 +1040,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         ++li;
     }
     if (pend.r >= 0) {
-        if (nobar) collect(P, S, pend, ct);
+        if (nobar && c > 1) collect_cluster(P, S, pend, ct, rank);
+        else if (nobar) collect(P, S, pend, ct);
         else if (c > 1) settle<OP>(P, S, pend, ct, rank);
         if (kKL && sizeof(T) == 2 && ct == 0) {
             const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
