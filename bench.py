@@ -106,6 +106,65 @@ def head_gemm_line(torch, flush, M=2048, N=128256, K=4096, reps=10):
     return out
 
 
+def head_pipeline_lines(torch, flush, reps=5):
+    """The head pipelines on the device, step by step: the student's (vl_head_kl: logits GEMM,
+    one-pass CE + top-k KL in place, dx GEMM over the transposed weight plane) on 2048 rows of
+    hidden size 4096 against a 32000 vocabulary, k 64; the teacher's (vl_teacher_topk: logits
+    GEMM, streaming top-k) on 2048 rows against a 128256 vocabulary, k 256; chunks of 1024
+    rows.  Each step timed alone after an L2 flush; `gemm_tflops` is the GEMMs' FLOPs over the
+    whole step's time (the loss or top-k kernels included)."""
+    from top_kl_distill_gb300 import vloss as vl
+    g = torch.Generator(device="cuda").manual_seed(20261)
+    n, hs = 2048, 4096
+
+    def bf16(rows, cols, scale):
+        return (torch.randn(rows, cols, device="cuda", generator=g) * scale).to(torch.bfloat16)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ms = []
+        for _ in range(reps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return sorted(ms)[len(ms) // 2]
+
+    out = {}
+    hidden = bf16(n, hs, 1.0)
+    V, k = 32000, 64
+    w = bf16(V, hs, 3.0 / hs ** 0.5)
+    wt = w.t().contiguous()
+    lab = _dev(torch, W.random_labels(n, V, seed=31))
+    tid, tp = W.random_teacher(n, V, k, seed=32)
+    tid, tp = _dev(torch, tid), _dev(torch, tp)
+    dx = torch.empty(n, hs, device="cuda")
+    kl, ce, mean = (torch.empty(n, device="cuda"), torch.empty(n, device="cuda"), torch.empty(1, device="cuda"))
+    ms = timed(lambda: vl.vl_head_kl(hidden, hs, w, wt, V, n, lab, tid, tp, k, 1.0 / n, 1.0 / n, 1.0, 0, n, dx, kl,
+                                     ce, mean))
+    out["head_kl"] = {"shape": f"{n} rows, hidden {hs}, V {V}, k {k}", "ms_per_step": round(ms, 4),
+                      "rows_per_s": round(n / (ms * 1e-3), 1),
+                      "gemm_tflops": round(2 * 2.0 * n * V * hs / (ms * 1e-3) / 1e12, 1), "gpu_launches": 9}
+    del w, wt, lab, tid, tp, dx, kl, ce, mean
+    torch.cuda.empty_cache()
+    V, k = 128256, 256
+    w = bf16(V, hs, 3.0 / hs ** 0.5)
+    ids = torch.empty(n, k, dtype=torch.int32, device="cuda")
+    probs = torch.empty(n, k, device="cuda")
+    ms = timed(lambda: vl.vl_teacher_topk(hidden, hs, w, V, n, k, 0, n, ids, probs))
+    out["teacher_topk"] = {"shape": f"{n} rows, hidden {hs}, V {V}, k {k}", "ms_per_step": round(ms, 4),
+                           "rows_per_s": round(n / (ms * 1e-3), 1),
+                           "gemm_tflops": round(2.0 * n * V * hs / (ms * 1e-3) / 1e12, 1), "gpu_launches": 6}
+    del w, ids, probs, hidden
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -1015,7 +1074,7 @@ def main():
         names = ["ce_tiny", "ce_lm_bf16", "kl", "topk_k256", "topk_k2048", "large_v", "large_v_bf16",
                  "large_v_sliced"]
         if args.sweep_only:
-            names = [n for n in args.sweep_only.split(",") if n and n != "head_gemm"]
+            names = [n for n in args.sweep_only.split(",") if n and n not in ("head_gemm", "head")]
         for name in names:
             c = make_case(torch, name, args.ntok or None, args.bufs or None)
             steps = args.sweep_steps
@@ -1036,6 +1095,8 @@ def main():
             torch.cuda.empty_cache()
         if not args.sweep_only or "head_gemm" in args.sweep_only.split(","):
             sweep["head_gemm"] = head_gemm_line(torch, flush)
+        if not args.sweep_only or "head" in args.sweep_only.split(","):
+            sweep.update(head_pipeline_lines(torch, flush))
         line["sweep"] = sweep
 
     if pool is not None:
