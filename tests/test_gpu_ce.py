@@ -220,3 +220,44 @@ def test_ce_fused_bad_labels_counted_once_per_row():
     oloss, olse, og, _ = O.ce_fused(x, np.where(lab < V, lab, 0).astype(np.uint32), 0, ntok, 0.5)
     H.check_loss(l[ok], oloss[ok], olse[ok])
     H.check_grad(H.host(view)[ok], og[ok], 0.5)
+
+
+def test_ce_fused_long_rows_on_clusters():
+    """Rows of 128256 fp32 columns: the fused CE splits each row over a cluster of CTAs, every
+    warp sending its pass A partial to every rank; a window, a ragged stride, a misaligned base,
+    two calls in a row."""
+    ntok, V, ld, off = 41, 128256, 128263, 3
+    x = W.random_logits(ntok, V, seed=777, sigma=2.0)
+    lab = W.random_labels(ntok, V, seed=778)
+    ls, le, scale = 5, 37, 1.0 / 32
+    oloss, olse, og, omean = O.ce_fused(x, lab, ls, le, scale)
+    for _ in range(2):
+        buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
+        g = H.host(view)
+        H.check_grad(g[:, :V], og, scale, "long-row gradient")
+        assert np.isnan(g[:, V:]).all()
+        assert np.isnan(H.host(buf)[:off]).all()
+        H.check_loss(H.host(loss), oloss, olse, "long-row loss")
+        H.check_lse(H.host(lse), olse, "long-row lse")
+        assert np.array_equal(H.host(stats)[:, 0], x.max(axis=1))
+        H.check_mean(H.host(mean)[0], omean)
+        assert int(H.host(err)[0]) == 0
+
+
+@pytest.mark.parametrize("jump", [30.0, 62.0, 66.0, 89.5, 90.5, 120.0, 300.0])
+def test_ce_fused_running_max_jumps(jump):
+    """A value far above everything before it in its row, in a later tile: the thread that
+    meets it raises its running max by about `jump` - 2 (its earlier values are N(0, 1)), so
+    the pass-A sum is rescaled (a small rise) or summed again against the new max (a rise of
+    64 or more, where the rescale factor would leave the normal range).  lse, loss and
+    gradient against the oracle."""
+    ntok, V, scale = 8, 20000, 0.125
+    x = W.random_logits(ntok, V, seed=int(jump * 10), sigma=1.0)
+    x[np.arange(ntok), 15000 + 7 * np.arange(ntok)] = np.float32(jump)
+    lab = W.random_labels(ntok, V, seed=int(jump * 10) + 1)
+    _, view, loss, lse, _, _, err = run_fused(x, lab, 0, ntok, scale)
+    oloss, olse, og, _ = O.ce_fused(x, lab, 0, ntok, scale)
+    H.check_grad(H.host(view), og, scale, f"gradient, jump {jump}")
+    H.check_loss(H.host(loss), oloss, olse, f"loss, jump {jump}")
+    H.check_lse(H.host(lse), olse, f"lse, jump {jump}")
+    assert int(H.host(err)[0]) == 0
