@@ -74,6 +74,8 @@ def _vl():
     (9, 7, 9, 2, 1, 8, 2.0),                # rows shorter than a 16-byte chunk
     (6, 1, 1, 0, 0, 6, 1.0),
     (5, 100003, 100003, 0, 0, 5, 3.0),      # a cluster of CTAs per row
+    (160, 5003, 5011, 1, 3, 150, 3.0),      # 2-CTA clusters, whole rows and split odd rows
+    (200, 33, 37, 3, 10, 190, 2.0),         # the same with rows of a few chunks
 ])
 def test_ce_fused_bf16(ntok, V, ld, off, ls, le, sigma):
     torch = H.torch_cuda()

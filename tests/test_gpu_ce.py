@@ -76,6 +76,42 @@ def test_ce_fused(name):
     assert int(H.host(err)[0]) == 0
 
 
+# Past two rows a pair of SMs the fused CE runs on 2-CTA clusters: each CTA takes whole rows
+# of its cluster's block, and an odd block's last row is split over the pair.  Bad labels
+# sit on rows of both kinds (row 5 is split when the device holds 76 such clusters).
+@pytest.mark.parametrize("ntok,V,ld,off,ls,le", [
+    (160, 5003, 5011, 1, 3, 150),     # misaligned rows: every row its own head and tail
+    (311, 4096, 4096, 0, 0, 311),     # aligned rows, 5 or 4 a cluster
+    (200, 33, 37, 2, 10, 190),        # rows of a few chunks
+])
+def test_ce_fused_pairs(ntok, V, ld, off, ls, le):
+    scale = 1.0 / (le - ls)
+    x = W.random_logits(ntok, V, seed=ntok * 7 + V, sigma=3.0)
+    lab = W.random_labels(ntok, V, seed=ntok * 7 + V + 1)
+    bad = [5, 12, ntok - 2]
+    lab[bad] = [V, V + 7, 0xFFFFFFFF]
+    buf, view, loss, lse, stats, mean, err = run_fused(x, lab, ls, le, scale, ld, off)
+    inwin = [t for t in bad if ls <= t < le]
+    assert int(H.host(err)[0]) == len(inwin)
+    fixed = np.where(lab < V, lab, 0).astype(np.uint32)
+    oloss, olse, og, _ = O.ce_fused(x, fixed, ls, le, scale)
+    ok = np.setdiff1d(np.arange(ntok), inwin)
+    l = H.host(loss)
+    H.check_loss(l[ok], oloss[ok], olse[ok])
+    assert all(np.isnan(l[t]) for t in inwin)
+    H.check_lse(H.host(lse), olse)
+    st = H.host(stats)
+    assert np.array_equal(st[:, 0], x.max(axis=1)), "stats[:, 0] is the exact row max"
+    g = H.host(view)
+    H.check_grad(g[ok, :V], og[ok], scale)
+    for t in inwin:      # a bad label leaves the softmax part of the gradient
+        H.check_grad(g[t, :V], scale * np.exp(x[t].astype(np.float64) - olse[t]), scale)
+    if ld > V:
+        assert np.isnan(g[:, V:]).all(), "columns past V were written"
+    if off:
+        assert np.isnan(H.host(buf)[:off]).all(), "memory before the first row was written"
+
+
 def test_ce_lm_peaky_rows():
     w = W.WORKLOADS["ce_lm"].scaled(96)
     w = W.Workload(**{**w.__dict__, "window": (16, 96)})

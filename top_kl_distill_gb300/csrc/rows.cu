@@ -6,6 +6,9 @@
 // Layout of one launch
 //   * grid = nclusters * csize CTAs, one CTA per SM (the ring below takes
 //     ~200 KB of shared memory).  Cluster i handles rows i, i + nclusters, ...
+//     A mixed launch (fused CE, 2-CTA clusters) gives cluster i a block of consecutive
+//     rows instead: each CTA takes every other row whole, and an odd block's last row
+//     is split over the pair, so that no CTA carries more than half a row above another.
 //   * a row slice of ncols elements is cut into a head (the elements before the first
 //     16-byte boundary: at most 3 fp32 or 7 bf16), a 16-byte-aligned body and a tail
 //     of the same bound.  The body is split evenly (in 16-byte chunks) across the csize
@@ -19,8 +22,9 @@
 //   self-contained (CE fused, KL without given statistics): the producer streams
 //             each row part twice.  Pass A reduces (max, sum of exponentials)
 //             online per thread; partials are merged across warps (shared
-//             memory) and across the cluster (distributed shared memory: st.async
-//             that completes the peer's mbarrier transaction count).  Pass B
+//             memory: for CE each warp publishes its partial and one warp, in turn,
+//             combines them) and across the cluster (distributed shared memory:
+//             st.async that completes the peer's mbarrier transaction count).  Pass B
 //             re-reads the part -- it was read microseconds earlier, so the bytes
 //             come from L2 -- and writes the gradient tile by tile.  HBM sees one
 //             read and one write per element; no row has to fit on chip.
@@ -156,6 +160,8 @@ struct alignas(128) Smem {
     float4 wred[2][NCW];                // per warp: (max, sum, KL a, KL b)
     uint64_t abar[kPartBufs];           // self-contained CE: every warp's pass A partial is in
     float2 wpart[kPartBufs][NCW];
+    uint64_t sbar[kPartBufs];           // self-contained CE: the row's statistics are in
+    float2 rstat[kPartBufs];            // (max, ln sum) of the row
     float wloss[2][NCW];
     union {
         struct {                        // streaming mode: support of the current row
@@ -200,7 +206,7 @@ __device__ __forceinline__ Part part_of(const T* rowp, int n, int rank, int c) {
     int h = (NV - mis) & (NV - 1);
     if (h > n) h = n;
     const int bt = (n - h) & ~(NV - 1);
-    const int per = ((bt / NV + c - 1) / c) * NV;
+    const int per = c == 1 ? bt : ((bt / NV + c - 1) / c) * NV;
     const int s = min(rank * per, bt);
     const int e = min((rank + 1) * per, bt);
     p.h = h;
@@ -244,36 +250,66 @@ __device__ __forceinline__ float soft(float s, float m, float lnS) {
     return ex2(((s - m) - lnS) * kLog2e);
 }
 
-// (max, sum) update with kVec chunks of NV values (absent values are -inf): one max
-// update, independent exponentials summed as a tree.
+// (max, sum) update with a whole tile's kVec chunks of NV values: one max update (a
+// tree of maxima), independent exponentials summed as a tree.
 template <int NV>
 __device__ __forceinline__ void ms_addv(MaxSum& a, const float (&v)[kVec][NV]) {
-    float mx = v[0][0];
+    constexpr int N = kVec * NV;
+    static_assert((N & (N - 1)) == 0, "a power of two values a tile");
+    float t[N];
 #pragma unroll
     for (int u = 0; u < kVec; ++u)
 #pragma unroll
-        for (int i = 0; i < NV; ++i) mx = fmaxf(mx, v[u][i]);
+        for (int i = 0; i < NV; ++i) t[u * NV + i] = v[u][i];
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    const float mx = t[0];
     if (mx > a.m) {
         a.s *= ex2((a.m - mx) * kLog2e);
         a.m = mx;
     }
-    float e[kVec];
+    float e[N / 2];
 #pragma unroll
-    for (int u = 0; u < kVec; ++u) {
-        float q[NV / 2];
+    for (int u = 0; u < kVec; ++u)
 #pragma unroll
         for (int i = 0; i < NV / 2; ++i)
-            q[i] = ex2((v[u][2 * i] - a.m) * kLog2e) + ex2((v[u][2 * i + 1] - a.m) * kLog2e);
+            e[u * (NV / 2) + i] = ex2((v[u][2 * i] - a.m) * kLog2e) + ex2((v[u][2 * i + 1] - a.m) * kLog2e);
 #pragma unroll
-        for (int w = NV / 4; w > 0; w >>= 1)
+    for (int w = N / 4; w > 0; w >>= 1)
 #pragma unroll
-            for (int i = 0; i < w; ++i) q[i] += q[i + w];
-        e[u] = q[0];
+        for (int i = 0; i < w; ++i) e[i] += e[i + w];
+    a.s += e[0];
+}
+
+// The same update with one chunk.
+template <int NV>
+__device__ __forceinline__ void ms_add_chunk(MaxSum& a, const float (&v)[NV]) {
+    float mx = v[0];
+#pragma unroll
+    for (int i = 1; i < NV; ++i) mx = fmaxf(mx, v[i]);
+    if (mx > a.m) {
+        a.s *= ex2((a.m - mx) * kLog2e);
+        a.m = mx;
     }
-    float t = e[0];
+    float e = 0.f;
 #pragma unroll
-    for (int u = 1; u < kVec; ++u) t += e[u];
-    a.s += t;
+    for (int i = 0; i < NV; ++i) e += ex2((v[i] - a.m) * kLog2e);
+    a.s += e;
+}
+
+// A tile of n16 chunks: thread ct holds chunks u * NCT + ct.  A row's last tile is
+// usually partial; its absent chunks are skipped rather than summed as -inf.
+template <int NV>
+__device__ __forceinline__ void ms_add_tile(MaxSum& a, const float (&v)[kVec][NV], int n16, int ct) {
+    if (n16 >= kVec * NCT) {
+        ms_addv<NV>(a, v);
+        return;
+    }
+#pragma unroll
+    for (int u = 0; u < kVec; ++u)
+        if (u * NCT + ct < n16) ms_add_chunk<NV>(a, v[u]);
 }
 
 // Chunk j of tile `slot` into v (absent chunks: -inf).
@@ -288,6 +324,41 @@ __device__ __forceinline__ void load_chunk(const Smem& S, uint32_t slot, int j, 
 }
 
 // ---------------------------------------------------------------- producer
+
+// Row item i of this CTA: the row, and which part of it (part prank of pc) the CTA takes.
+// Plain launches walk rows cid, cid + ncl, ... whole (pc = 1) or split over the cluster.
+// Mixed launches (2-CTA clusters) give cluster cid a block of consecutive rows; an odd
+// block's last row comes first and is split over the pair, then each CTA takes every other
+// row of the block whole.  A CTA then carries at most half a row more than another.
+struct Item {
+    long long r;
+    int prank, pc;
+};
+
+__device__ __forceinline__ bool row_item(const RowParams& P, int rank, long long cid, long long ncl, long long i,
+                                         Item& it) {
+    if (!P.mixed) {
+        it.r = P.rbeg + cid + i * ncl;
+        it.prank = rank;
+        it.pc = P.csize;
+        return it.r < P.rend;
+    }
+    const long long R = P.rend - P.rbeg, q = R / ncl, rm = R % ncl;
+    const long long nk = q + (cid < rm ? 1 : 0);
+    const long long base = P.rbeg + cid * q + (cid < rm ? cid : rm);
+    const long long odd = nk & 1;
+    if (odd && i == 0) {
+        it.r = base + nk - 1;
+        it.prank = rank;
+        it.pc = 2;
+        return true;
+    }
+    const long long j = i - odd;
+    it.r = base + 2 * j + rank;
+    it.prank = 0;
+    it.pc = 1;
+    return j < nk / 2;
+}
 
 // Issue the body tiles of one row part; false if a wait gave up.
 template <typename T>
@@ -306,9 +377,9 @@ __device__ __forceinline__ bool issue_body(const RowParams& P, Smem& S, const T*
 }
 
 template <typename T>
-__device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long long r, int rank, uint32_t& g) {
-    const T* rowp = row_ptr<T>(P, r);
-    return issue_body<T>(P, S, rowp, part_of<T>(rowp, (int)P.ncols, rank, P.csize), g);
+__device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, const Item& it, uint32_t& g) {
+    const T* rowp = row_ptr<T>(P, it.r);
+    return issue_body<T>(P, S, rowp, part_of<T>(rowp, (int)P.ncols, it.prank, it.pc), g);
 }
 
 // Tile order: one pass per row for the streaming and reduce modes; for the
@@ -317,16 +388,17 @@ __device__ __forceinline__ bool issue_part(const RowParams& P, Smem& S, long lon
 template <typename T, int OP, bool RES>
 __device__ void producer(const RowParams& P, Smem& S, int rank, long long cid, long long ncl) {
     uint32_t g = 0;
-    long long prev = -1;
-    for (long long r = P.rbeg + cid; r < P.rend; r += ncl) {
-        if (!row_loaded<OP>(P, r)) continue;
-        if (!issue_part<T>(P, S, r, rank, g)) break;
+    Item it, prev;
+    prev.r = -1;
+    for (long long i = 0; row_item(P, rank, cid, ncl, i, it); ++i) {
+        if (!row_loaded<OP>(P, it.r)) continue;
+        if (!issue_part<T>(P, S, it, g)) break;
         if (RES) {
-            if (prev >= 0 && !issue_part<T>(P, S, prev, rank, g)) break;
-            prev = r;
+            if (prev.r >= 0 && !issue_part<T>(P, S, prev, g)) break;
+            prev = it;
         }
     }
-    if (RES && prev >= 0 && !S.abort) issue_part<T>(P, S, prev, rank, g);
+    if (RES && prev.r >= 0 && !S.abort) issue_part<T>(P, S, prev, g);
     S.issued = g;
 }
 
@@ -378,14 +450,26 @@ __device__ __forceinline__ void gather_support(Smem& S, uint32_t kb, const int (
             S.ks[kb][ct + i * NCT] = Elem<T>::get(reinterpret_cast<const T*>(tile) + erel[i] % kTileE<T>);
 }
 
-// (max, sum) of n partials: the max first, then the sums rescaled independently.
-__device__ __forceinline__ MaxSum combine(const float2* part, int n) {
-    float M = part[0].x;
-    for (int i = 1; i < n; ++i) M = fmaxf(M, part[i].x);
+// (max, sum) of n <= 128 partials, by one warp: lane i takes partials i, i + 32, ...; the
+// max and then the rescaled sums meet in butterflies, which leave every lane (and every
+// warp that runs this on the same partials) with the same bits.
+__device__ __forceinline__ MaxSum combine_warp(const float2* part, int n, int lane) {
+    float2 q[4];
+    float M = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = lane + 32 * i;
+        q[i] = j < n ? part[j] : make_float2(-FLT_MAX, 0.f);
+        M = fmaxf(M, q[i].x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float T = 0.f;
-    for (int i = 0; i < n; ++i) T += part[i].y * ex2((part[i].x - M) * kLog2e);
-    return MaxSum{M, T};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) T += q[i].y * ex2((q[i].x - M) * kLog2e);
+    return MaxSum{M, warp_sum(T)};
 }
+static_assert(kMaxCluster * NCW <= 128, "combine_warp takes up to 128 partials");
 
 // Row partials with the KL loss parts: (max, sum) combined as above, and the sums
 // a = sum p (ln p - s), b = sum p over the teacher support entries the parts hold.
@@ -518,7 +602,7 @@ __device__ void consumer(const RowParams& P, Smem& S, int rank, long long cid, l
                 if (ct == LT) gather<T>(lab, t, S.ring[slot]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[slot]);
-                ms_addv<NV>(ms, v);
+                ms_add_tile<NV>(ms, v, n16, ct);
             }
             g += (uint32_t)nt;
             ms = ms_warp_reduce(ms);
@@ -662,13 +746,15 @@ struct Pending {
     float m, lnS;
     float ht;        // the logit at jht
     // bit 0 in the window, bit 1 bad label, bit 2 this part holds column 0 of the row (it
-    // writes lse, stats and the out-of-window loss); bits 8-9 the cluster exchange buffer of
+    // writes lse, stats and the out-of-window loss), bit 3 the row is split over the cluster;
+    // bits 8-9 the cluster exchange buffer of
     // the row's statistics and bit 10 the phase to wait for; bits 16-19 the buffer of the
     // warps' pass A partials (CE) and bit 20 its phase
     uint32_t f;
     __device__ __forceinline__ bool inwin() const { return f & 1u; }
     __device__ __forceinline__ bool bad() const { return f & 2u; }
     __device__ __forceinline__ bool first() const { return f & 4u; }
+    __device__ __forceinline__ bool shared() const { return f & 8u; }
     __device__ __forceinline__ uint32_t xb() const { return (f >> 8) & 3u; }
     __device__ __forceinline__ uint32_t xpar() const { return (f >> 10) & 1u; }
     __device__ __forceinline__ uint32_t ab() const { return (f >> 16) & 15u; }
@@ -678,7 +764,8 @@ struct Pending {
 // Pass B of a row whose statistics are known: the gradient tile by tile with the
 // label's one-hot folded in.  The teacher support is left to scatter_support.
 template <typename T, int OP>
-__device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane) {
+__device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pending& w, uint32_t& g, int ct, int lane,
+                                       float l2cg) {
     constexpr int NV = Elem<T>::NV;
     T* const rowp = row_ptr<T>(P, w.r);
     const int nt = (w.bn + kTileE<T> - 1) / kTileE<T>;
@@ -689,41 +776,48 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     // the gradient lines are done with: written back first, ahead of the logits that
     // pass B of the next row still re-reads from L2
     const uint64_t pol = l2_evict_first();
-    const float K = fold ? w.lnS * kLog2e - log2f(c1) : 0.f;
+    const float K = fold ? w.lnS * kLog2e - (w.inwin() ? l2cg : -INFINITY) : 0.f;
     for (int t = 0; t < nt; ++t) {
         const uint32_t gt = g + (uint32_t)t, slot = gt % kSlots;
         wait_parity<false>(&S.full[slot], (gt / kSlots) & 1u, &S.abort, &g_watchdog, P.wait_limit);
         const int n16 = min(kTileE<T>, w.bn - t * kTileE<T>) / NV;
-        uint4 raw[kVec];
-#pragma unroll
-        for (int u = 0; u < kVec; ++u) {
+        auto grad = [&](int u, uint4 raw) {
             const int j = u * NCT + ct;
-            if (j < n16) raw[u] = ld_shared_u4(&S.ring[slot][16 * j]);
-        }
+            const int c0 = w.b0 + t * kTileE<T> + NV * j;
+            float x[NV], o[NV];
+            Elem<T>::unpack(raw, x);
+            grad_chunk<NV>(x, o, fold, w.m, w.lnS, K, c1);
+            if (w.inwin()) {
+                const unsigned d = (unsigned)(w.jl - c0);
+                if (d < (unsigned)NV) {
+#pragma unroll
+                    for (int i = 0; i < NV; ++i)
+                        if ((unsigned)i == d) {
+                            o[i] -= P.ce_coef;
+                            if (ce_out) ce_out[w.r] = (w.m - x[i]) + w.lnS;
+                        }
+                }
+            }
+            st_global_u4_hint(rowp + c0, Elem<T>::pack(o), pol);
+        };
+        // half the tile's chunks turned into gradient while the other half is still in the
+        // slot; the slot is released once the second half is in registers
+        constexpr int H = kVec / 2;
+        uint4 raw[H];
+#pragma unroll
+        for (int u = 0; u < H; ++u)
+            if (u * NCT + ct < n16) raw[u] = ld_shared_u4(&S.ring[slot][16 * (u * NCT + ct)]);
+#pragma unroll
+        for (int u = 0; u < H; ++u)
+            if (u * NCT + ct < n16) grad(u, raw[u]);
+#pragma unroll
+        for (int u = 0; u < H; ++u)
+            if ((H + u) * NCT + ct < n16) raw[u] = ld_shared_u4(&S.ring[slot][16 * ((H + u) * NCT + ct)]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) {
-            const int j = u * NCT + ct;
-            if (j < n16) {
-                const int c0 = w.b0 + t * kTileE<T> + NV * j;
-                float x[NV], o[NV];
-                Elem<T>::unpack(raw[u], x);
-                grad_chunk<NV>(x, o, fold, w.m, w.lnS, K, c1);
-                if (w.inwin()) {
-                    const unsigned d = (unsigned)(w.jl - c0);
-                    if (d < (unsigned)NV) {
-#pragma unroll
-                        for (int i = 0; i < NV; ++i)
-                            if ((unsigned)i == d) {
-                                o[i] -= P.ce_coef;
-                                if (ce_out) ce_out[w.r] = (w.m - x[i]) + w.lnS;
-                            }
-                    }
-                }
-                st_global_u4_hint(rowp + c0, Elem<T>::pack(o), pol);
-            }
-        }
+        for (int u = 0; u < H; ++u)
+            if ((H + u) * NCT + ct < n16) grad(H + u, raw[u]);
     }
     g += (uint32_t)nt;
     if (w.jht >= 0) {
@@ -740,16 +834,26 @@ __device__ __forceinline__ void pass_b(const RowParams& P, Smem& S, const Pendin
     }
 }
 
-// Self-contained CE, one CTA per row: the row's statistics from the warps' partials.
-__device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w, int ct) {
+// Self-contained CE, one CTA per row: one warp (the row's collector, in turn) combines the
+// warps' pass A partials once all are in and publishes the row's statistics; the other
+// warps only read them, a row later, before the row's pass B.
+__device__ __forceinline__ void collect_row(const RowParams& P, Smem& S, const Pending& w, int lane) {
     wait_parity<false>(&S.abar[w.ab()], w.apar(), &S.abort, &g_watchdog, P.wait_limit);
-    const MaxSum tot = combine(S.wpart[w.ab()], NCW);
-    w.m = tot.m;
-    w.lnS = logf(tot.s);
-    if (ct == LT) {
-        if (P.lse_out) P.lse_out[w.r] = w.m + w.lnS;
-        if (P.stats_out) { P.stats_out[2 * w.r] = w.m; P.stats_out[2 * w.r + 1] = w.lnS; }
+    const MaxSum tot = combine_warp(S.wpart[w.ab()], NCW, lane);
+    const float lnS = logf(tot.s);
+    if (lane == 0) {
+        S.rstat[w.ab()] = make_float2(tot.m, lnS);
+        mbar_arrive(&S.sbar[w.ab()]);
+        if (P.lse_out) P.lse_out[w.r] = tot.m + lnS;
+        if (P.stats_out) { P.stats_out[2 * w.r] = tot.m; P.stats_out[2 * w.r + 1] = lnS; }
     }
+}
+
+__device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w) {
+    wait_parity<false>(&S.sbar[w.ab()], w.apar(), &S.abort, &g_watchdog, P.wait_limit);
+    const float2 st = S.rstat[w.ab()];
+    w.m = st.x;
+    w.lnS = st.y;
 }
 
 // Self-contained CE over a cluster: the row's statistics from every warp of every rank,
@@ -757,7 +861,7 @@ __device__ __forceinline__ void collect(const RowParams& P, Smem& S, Pending& w,
 // (rank, then warp), so all hold the same bits.
 __device__ __forceinline__ void collect_cluster(const RowParams& P, Smem& S, Pending& w, int ct, int rank) {
     wait_parity<true>(&S.xbar[w.xb()], w.xpar(), &S.abort, &g_watchdog, P.wait_limit);
-    const MaxSum tot = combine(&S.xw[w.xb()][0][0], P.csize * NCW);
+    const MaxSum tot = combine_warp(&S.xw[w.xb()][0][0], P.csize * NCW, ct & 31);
     w.m = tot.m;
     w.lnS = logf(tot.s);
     if (rank == 0 && ct == LT) {
@@ -827,7 +931,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const int ncols = (int)P.ncols;
     const bool has_label = (OP != kKl) || P.labels != nullptr;
     // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
-    const bool nobar = !kKL && ncols >= 2 * NV * c;
+    const bool nobar = !kKL && ncols >= 2 * NV * c;   // mixed launches: c = 2 covers the whole rows too
+    const float l2cg = log2f(P.cg);   // the gradient scale folded into pass B's exponent
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
     long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (support scatter owed)
     uint32_t nlab = 0, nid = 0;
@@ -837,24 +942,31 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         if (has_label) nlab = P.labels[rr];
         if (kKL && ct < P.k) { nid = P.tid[rr * P.k + ct]; np = P.tp[rr * P.k + ct]; }
     };
-    prefetch(P.rbeg + cid);
+    Item it, nx_it;
+    const bool any = row_item(P, rank, cid, ncl, 0, nx_it);
+    if (any) prefetch(nx_it.r);
     Pending pend;
     pend.r = -1;
 
-    for (long long r = P.rbeg + cid; r < P.rend; r += ncl) {
+    for (long long ii = 0; any; ++ii) {
+        it = nx_it;
+        const long long r = it.r;
+        const bool more = row_item(P, rank, cid, ncl, ii + 1, nx_it);
         const uint32_t lab_r = nlab, id0 = nid;
         const float p0 = np;
-        prefetch(r + ncl);
+        if (more) prefetch(nx_it.r);
         T* rowp = row_ptr<T>(P, r);
-        const Part pt = part_of<T>(rowp, ncols, rank, c);
+        const Part pt = part_of<T>(rowp, ncols, it.prank, it.pc);
         const bool inwin = r >= P.ls && r < P.le;
+        const bool shared = it.pc > 1;
         if (!row_loaded<OP>(P, r)) {
             zero_part<T>(rowp, pt, ct);
-            if (ct == 0 && rank == 0) {
+            if (ct == 0 && it.prank == 0) {
                 P.loss[r] = 0.f;
                 if (P.ce_loss) P.ce_loss[r] = 0.f;
             }
-            continue;
+            if (more) continue;
+            break;
         }
         const uint32_t sb = li % kSupBufs;
         Pending cur;
@@ -871,8 +983,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                 if (j >= pt.lo && j < pt.hi) cur.jl = (int)j;
             }
         }
-        cur.f = (inwin ? 1u : 0u) | (bad ? 2u : 0u) | (rank == 0 ? 4u : 0u);
-        if (bad && inwin && rank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
+        cur.f = (inwin ? 1u : 0u) | (bad ? 2u : 0u) | (it.prank == 0 ? 4u : 0u) | (shared ? 8u : 0u);
+        if (bad && inwin && it.prank == 0 && ct == LT && P.err) atomicAdd(P.err, 1);
         // teacher support entries q = ct + i * NCT: column and probability to shared
         // memory for the scatter, the logit gathered now -- nothing of the row is
         // written before the barrier that ends its pass A -- for the loss
@@ -893,7 +1005,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                     const float p = i == 0 ? p0 : P.tp[r * P.k + q];
                     int col = -1;
                     if ((long long)id >= P.V) {
-                        if (rank == 0 && P.err) atomicAdd(P.err, 1);
+                        if (it.prank == 0 && P.err) atomicAdd(P.err, 1);
                     } else {
                         const long long j = (long long)id - P.col0;
                         if (j >= pt.lo && j < pt.hi) col = (int)j;
@@ -922,11 +1034,11 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             for (int u = 0; u < kVec; ++u) load_chunk<T>(S, slot, u * NCT + ct, n16, v[u]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
-            ms_addv<NV>(ms, v);
+            ms_add_tile<NV>(ms, v, n16, ct);
         }
         g += (uint32_t)nt;
         ms = ms_warp_reduce(ms);
-        if (nobar && c > 1) {
+        if (nobar && shared) {
             // CE over a cluster: this warp's partial goes to every rank (st.async completing the
             // rank's exchange barrier, whose one local arrival carries the bytes expected); the
             // row is collected just before its pass B, one row later -- no CTA barrier per row.
@@ -941,30 +1053,35 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                     st_async_f32x2(map_to_rank(&S.xw[cur.xb()][rank][cw], (uint32_t)q), ms.m, ms.s,
                                    map_to_rank(&S.xbar[cur.xb()], (uint32_t)q));
             if (pend.r >= 0) {
-                collect_cluster(P, S, pend, ct, rank);
-                pass_b<T, OP>(P, S, pend, g, ct, lane);
+                if (pend.shared()) collect_cluster(P, S, pend, ct, rank);
+                else collect(P, S, pend);
+                pass_b<T, OP>(P, S, pend, g, ct, lane, l2cg);
             }
             pend = cur;
             ++li;
-            continue;
+            if (more) continue;
+            break;
         }
         if (nobar) {
             // CE: publish this warp's partial and move on; the row's statistics are
             // collected just before its pass B, one row later, when every warp has long
             // arrived -- no CTA-wide barrier per row
             cur.f |= ((nred % kPartBufs) << 16) | (((nred / kPartBufs) & 1u) << 20);
-            ++nred;
             if (lane == 0) {
                 S.wpart[cur.ab()][cw] = make_float2(ms.m, ms.s);
                 mbar_arrive(&S.abar[cur.ab()]);
             }
+            if (cw == (int)(nred % NCW)) collect_row(P, S, cur, lane);
+            ++nred;
             if (pend.r >= 0) {
-                collect(P, S, pend, ct);
-                pass_b<T, OP>(P, S, pend, g, ct, lane);
+                if (pend.shared()) collect_cluster(P, S, pend, ct, rank);
+                else collect(P, S, pend);
+                pass_b<T, OP>(P, S, pend, g, ct, lane, l2cg);
             }
             pend = cur;
             ++li;
-            continue;
+            if (more) continue;
+            break;
         }
         const uint32_t b = nred & 1u;
         ++nred;
@@ -989,7 +1106,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, ka, kb);
         named_sync(kBarConsumers, NCT);
         const Part4 tot = combine4(S.wred[b], NCW);
-        if (c > 1) {
+        if (shared) {
             // send this CTA's part to every rank; the parts are collected just before this
             // row's pass B, one row later, so the exchange overlaps the next pass A.  Four
             // buffers: a peer writes buffer i + 4 only after its own collection of row
@@ -1025,30 +1142,31 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         }
         // ---- pass B of the previous row
         if (pend.r >= 0) {
-            if (c > 1) settle<OP>(P, S, pend, ct, rank);
+            if (pend.shared()) settle<OP>(P, S, pend, ct, rank);
             if (kKL && sizeof(T) == 2 && ct == 0) {
                 // bf16: the row statistics for its support rewrite, two rows on
                 const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
                 S.erow[pb][0] = pend.m;
                 S.erow[pb][1] = pend.lnS;
             }
-            pass_b<T, OP>(P, S, pend, g, ct, lane);
+            pass_b<T, OP>(P, S, pend, g, ct, lane, l2cg);
         }
         pend = cur;
         rk2 = rk1;
         rk1 = r;
         ++li;
+        if (!more) break;
     }
     if (pend.r >= 0) {
-        if (nobar && c > 1) collect_cluster(P, S, pend, ct, rank);
-        else if (nobar) collect(P, S, pend, ct);
-        else if (c > 1) settle<OP>(P, S, pend, ct, rank);
+        if (nobar && pend.shared()) collect_cluster(P, S, pend, ct, rank);
+        else if (nobar) collect(P, S, pend);
+        else if (pend.shared()) settle<OP>(P, S, pend, ct, rank);
         if (kKL && sizeof(T) == 2 && ct == 0) {
             const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
             S.erow[pb][0] = pend.m;
             S.erow[pb][1] = pend.lnS;
         }
-        pass_b<T, OP>(P, S, pend, g, ct, lane);
+        pass_b<T, OP>(P, S, pend, g, ct, lane, l2cg);
     }
     if (kKL && li > 0) {
         named_sync(kBarConsumers, NCT);
@@ -1072,7 +1190,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
             mbar_init(&S.empty[s], NCW);
         }
         for (int b = 0; b < 4; ++b) mbar_init(&S.xbar[b], 1u);   // the local expect_tx; the peers' data completes the bytes
-        for (int b = 0; b < kPartBufs; ++b) mbar_init(&S.abar[b], NCW);
+        for (int b = 0; b < kPartBufs; ++b) {
+            mbar_init(&S.abar[b], NCW);
+            mbar_init(&S.sbar[b], 1);
+        }
         S.abort = 0;
         S.issued = 0;
         fence_mbar_init_cluster();

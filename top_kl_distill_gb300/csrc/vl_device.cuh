@@ -284,24 +284,19 @@ __device__ __forceinline__ void ms_add4(MaxSum& a, float4 v) {
            (ex2((v.z - a.m) * kLog2e) + ex2((v.w - a.m) * kLog2e));
 }
 
-__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
-    const float m = fmaxf(a.m, b.m);
-    return MaxSum{m, a.s * ex2((a.m - m) * kLog2e) + b.s * ex2((b.m - m) * kLog2e)};
-}
-
-__device__ __forceinline__ MaxSum ms_warp_reduce(MaxSum a) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        MaxSum b{__shfl_xor_sync(0xffffffffu, a.m, off), __shfl_xor_sync(0xffffffffu, a.s, off)};
-        a = ms_merge(a, b);
-    }
-    return a;
-}
-
 __device__ __forceinline__ float warp_sum(float a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
     return a;
+}
+
+// The warp's (max, sum): the max over the lanes first, then each lane's sum rescaled to
+// it once and summed (butterflies: every lane holds the same bits).
+__device__ __forceinline__ MaxSum ms_warp_reduce(MaxSum a) {
+    float M = a.m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    return MaxSum{M, warp_sum(a.s * ex2((a.m - M) * kLog2e))};
 }
 
 }  // namespace vl

@@ -31,6 +31,8 @@ struct RowParams {
     float* stats_out;
     int* err;
     int csize;                // CTAs per row (cluster size)
+    int mixed;                // fused CE on 2-CTA clusters: each CTA takes whole rows of its cluster's
+                              // block, and an odd block's last row is split over the pair
     long long wait_limit;     // SM cycles after which a wait gives up (normally about 2 s)
     long long withhold;       // test hook: body tile of CTA 0 the producer never issues (-1: none)
 };
@@ -39,10 +41,10 @@ enum RowOp : int { kCeFused = 0, kCeFwd = 1, kCeBwd = 2, kKl = 3 };
 
 // Row-engine geometry limits (rows.cu).
 constexpr int kConsumerWarps = 15;        // + one producer warp: 16 warps, up to 128 registers a thread
-constexpr int kVec = 2;                   // row engine: 16-byte chunks of each tile per consumer thread
-constexpr int kTileB = 16 * 32 * kConsumerWarps * kVec;  // bytes per pipeline tile (15 KB)
+constexpr int kVec = 4;                   // row engine: 16-byte chunks of each tile per consumer thread
+constexpr int kTileB = 16 * 32 * kConsumerWarps * kVec;  // bytes per pipeline tile (30 KB)
 constexpr int kTileF = kTileB / 4;        // fp32 elements per tile
-constexpr int kSlots = 12;                // tiles in the shared-memory ring (180 KB)
+constexpr int kSlots = 6;                 // tiles in the shared-memory ring (180 KB)
 constexpr int kMaxCluster = 8;
 
 // Launch `op` over P; `resident` selects the self-contained mode that computes the
