@@ -162,6 +162,8 @@ struct alignas(128) Smem {
     float2 wpart[kPartBufs][NCW];
     uint64_t sbar[kPartBufs];           // self-contained CE: the row's statistics are in
     float2 rstat[kPartBufs];            // (max, ln sum) of the row
+    float4 wpart4[kPartBufs][NCW];      // self-contained KL without a barrier: each warp's (max, sum, a, b)
+    uint64_t bdone[kSupBufs];           // ... every warp's pass B stores of the row are done
     float wloss[2][NCW];
     union {
         struct {                        // streaming mode: support of the current row
@@ -932,6 +934,12 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
     const bool has_label = (OP != kKl) || P.labels != nullptr;
     // barrier-free statistics (CE, one CTA per row, every row at least one body tile)
     const bool nobar = !kKL && ncols >= 2 * NV * c;   // mixed launches: c = 2 covers the whole rows too
+    // KL without a CTA barrier per row, when a row part spans at least four tiles a pass (a
+    // warp is then less than a row ahead of any other: the ring holds kSlots tiles).  Each
+    // warp publishes its partial on an mbarrier; one warp in turn combines them; the support
+    // scatter of a row waits for every warp's pass B of it on another.
+    const bool kfree = kKL && ncols >= 4 * c * kTileE<T>;
+    static_assert(4 * 2 > kSlots, "four tiles a pass keep the warps within a row of each other");
     const float l2cg = log2f(P.cg);   // the gradient scale folded into pass B's exponent
     uint32_t g = 0, nred = 0, nx = 0, li = 0;
     long long rk1 = -1, rk2 = -1;      // KL: the last two loaded rows (support scatter owed)
@@ -1084,6 +1092,8 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             break;
         }
         const uint32_t b = nred & 1u;
+        const uint32_t ab = nred % kPartBufs, apar = (nred / kPartBufs) & 1u;
+        const bool collector = cw == (int)(nred % NCW);
         ++nred;
         // KL loss parts of the support entries this thread holds: a = sum p (ln p - s),
         // b = sum p (the loss is a + lse * b; entries with p <= 0 add no term).  Formed
@@ -1103,9 +1113,22 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             ka = warp_sum(ka);
             kb = warp_sum(kb);
         }
-        if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, ka, kb);
-        named_sync(kBarConsumers, NCT);
-        const Part4 tot = combine4(S.wred[b], NCW);
+        Part4 tot{MaxSum{0.f, 0.f}, 0.f, 0.f};
+        if (kfree) {
+            cur.f |= (ab << 16) | (apar << 20);
+            if (lane == 0) {
+                S.wpart4[ab][cw] = make_float4(ms.m, ms.s, ka, kb);
+                mbar_arrive(&S.abar[ab]);
+            }
+            if (collector) {
+                wait_parity<false>(&S.abar[ab], apar, &S.abort, &g_watchdog, P.wait_limit);
+                tot = combine4(S.wpart4[ab], NCW);
+            }
+        } else {
+            if (lane == 0) S.wred[b][cw] = make_float4(ms.m, ms.s, ka, kb);
+            named_sync(kBarConsumers, NCT);
+            tot = combine4(S.wred[b], NCW);
+        }
         if (shared) {
             // send this CTA's part to every rank; the parts are collected just before this
             // row's pass B, one row later, so the exchange overlaps the next pass A.  Four
@@ -1113,12 +1136,23 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
             // i + 2, which needs this CTA's part of row i + 2, sent after row i was read.
             cur.f |= ((nx & 3u) << 8) | (((nx >> 2) & 1u) << 10);
             ++nx;
-            if (ct == 0) {
+            if (kfree ? collector && lane == 0 : ct == 0) {
                 mbar_arrive_expect_tx(&S.xbar[cur.xb()], 16u * (uint32_t)c);
                 const float4 mine = make_float4(tot.ms.m, tot.ms.s, tot.a, tot.b);
                 for (int q = 0; q < c; ++q)
                     st_async_f32x4(map_to_rank(&S.xbuf[cur.xb()][rank], (uint32_t)q), mine,
                                    map_to_rank(&S.xbar[cur.xb()], (uint32_t)q));
+            }
+        } else if (kfree) {
+            if (collector) {
+                const float lnS = logf(tot.ms.s);
+                if (lane == 0) {
+                    S.rstat[ab] = make_float2(tot.ms.m, lnS);
+                    mbar_arrive(&S.sbar[ab]);
+                    if (P.lse_out) P.lse_out[r] = tot.ms.m + lnS;
+                    if (P.stats_out) { P.stats_out[2 * r] = tot.ms.m; P.stats_out[2 * r + 1] = lnS; }
+                    P.loss[r] = fmaf(tot.ms.m + lnS, tot.b, tot.a);
+                }
             }
         } else {
             cur.m = tot.ms.m;
@@ -1129,8 +1163,14 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                 if (kKL) P.loss[r] = fmaf(cur.m + cur.lnS, tot.b, tot.a);
             }
         }
-        // past this row's barrier, pass B of the row two back is done: its support terms
-        if (kKL && rk2 >= 0) scatter_support<T>(P, S, rk2, (li + kSupBufs - 2u) % kSupBufs, ct);
+        // pass B of the row two back is done (past this row's barrier, or every warp has
+        // arrived for it): its support terms
+        if (kKL && rk2 >= 0) {
+            const uint32_t l2 = li - 2u;
+            if (kfree && ct < P.k)
+                wait_parity<false>(&S.bdone[l2 % kSupBufs], (l2 / kSupBufs) & 1u, &S.abort, &g_watchdog, P.wait_limit);
+            scatter_support<T>(P, S, rk2, l2 % kSupBufs, ct);
+        }
         // bf16: the label column of this row (slice coordinates; -1 none) for its rewrite
         if (kKL && sizeof(T) == 2 && ct == LT) {
             int jfull = -1;
@@ -1143,6 +1183,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         // ---- pass B of the previous row
         if (pend.r >= 0) {
             if (pend.shared()) settle<OP>(P, S, pend, ct, rank);
+            else if (kfree) collect(P, S, pend);
             if (kKL && sizeof(T) == 2 && ct == 0) {
                 // bf16: the row statistics for its support rewrite, two rows on
                 const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
@@ -1150,6 +1191,10 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
                 S.erow[pb][1] = pend.lnS;
             }
             pass_b<T, OP>(P, S, pend, g, ct, lane, l2cg);
+            if (kfree) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.bdone[(li - 1u) % kSupBufs]);
+            }
         }
         pend = cur;
         rk2 = rk1;
@@ -1161,6 +1206,7 @@ __device__ void consumer_self(const RowParams& P, Smem& S, int rank, long long c
         if (nobar && pend.shared()) collect_cluster(P, S, pend, ct, rank);
         else if (nobar) collect(P, S, pend);
         else if (pend.shared()) settle<OP>(P, S, pend, ct, rank);
+        else if (kfree) collect(P, S, pend);
         if (kKL && sizeof(T) == 2 && ct == 0) {
             const uint32_t pb = (li + kSupBufs - 1u) % kSupBufs;
             S.erow[pb][0] = pend.m;
@@ -1194,6 +1240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) row_kernel(const __grid_constant_
             mbar_init(&S.abar[b], NCW);
             mbar_init(&S.sbar[b], 1);
         }
+        for (int b = 0; b < (int)kSupBufs; ++b) mbar_init(&S.bdone[b], NCW);
         S.abort = 0;
         S.issued = 0;
         fence_mbar_init_cluster();
