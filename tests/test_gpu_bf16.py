@@ -142,6 +142,7 @@ def test_ce_fwd_then_sliced_bwd_bf16():
     (23, 4099, 4103, 5, 37, True),          # repeated ids, a misaligned base
     (6, 2048, 2048, 0, 1024, False),        # the largest support
     (4, 100003, 100003, 1, 128, True),      # a cluster of CTAs per row
+    (300, 70001, 70009, 3, 64, True),       # rows of four tiles and more, more rows than SMs
 ])
 def test_kl_self_contained_bf16(ntok, V, ld, off, k, dup):
     torch = H.torch_cuda()

@@ -96,6 +96,33 @@ def test_kl_with_ce_fold_self_contained():
     H.check_loss(H.host(loss), oloss, _lse(x), "KL")
 
 
+def test_kl_many_rows_a_cta():
+    """Rows of four tiles and more, more rows than SMs: the self-contained KL runs without a
+    CTA barrier per row (partials and pass-B completion on mbarriers, one warp in turn
+    combining).  Repeated ids, zero probabilities, bad ids and folded labels, misaligned."""
+    ntok, V, ld, off, k = 400, 32003, 32009, 1, 64
+    x = W.random_logits(ntok, V, seed=41, sigma=2.5)
+    tid, tp = W.random_teacher(ntok, V, k, seed=42)
+    lab = W.random_labels(ntok, V, seed=43)
+    tid[:, 5] = tid[:, 9]
+    tid[:, 6] = lab
+    tp[:, 11] = 0.0
+    tid[7, 3] = V + 1
+    tid[250, 0] = 0xFFFFFFFF
+    coef, ce_coef = 1.0 / ntok, 0.5 / ntok
+    buf, view, loss, err = run_kl(x, tid, tp, coef, 0, ntok, ld, off, labels=lab, ce_coef=ce_coef)
+    assert int(H.host(err)[0]) == 2
+    keep = tid < V
+    tp_o = np.where(keep, tp, 0.0)
+    tid_o = np.where(keep, tid, 0).astype(np.uint32)
+    oloss, og = O.kl_topk(x, tid_o, tp_o, coef, labels=lab, ce_coef=ce_coef)
+    g = H.host(view)
+    H.check_grad(g[:, :V], og, coef + ce_coef)
+    assert np.isnan(g[:, V:]).all()
+    assert np.isnan(H.host(buf)[:off]).all()
+    H.check_loss(H.host(loss), oloss, _lse(x), "KL")
+
+
 @pytest.mark.parametrize("use_stats", [True, False])
 def test_large_vocab_sliced_step(use_stats):
     """The large-vocabulary step at 16 rows: CE forward over full rows, then per vocabulary
