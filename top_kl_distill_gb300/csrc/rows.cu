@@ -22,8 +22,9 @@
 //   self-contained (CE fused, KL without given statistics): the producer streams
 //             each row part twice.  Pass A reduces (max, sum of exponentials)
 //             online per thread; partials are merged across warps (shared
-//             memory: for CE each warp publishes its partial and one warp, in turn,
-//             combines them) and across the cluster (distributed shared memory:
+//             memory: for CE, and for KL rows of four tiles a pass or more, each warp
+//             publishes its partial and one warp, in turn, combines them) and across
+//             the cluster (distributed shared memory:
 //             st.async that completes the peer's mbarrier transaction count).  Pass B
 //             re-reads the part -- it was read microseconds earlier, so the bytes
 //             come from L2 -- and writes the gradient tile by tile.  HBM sees one
@@ -32,13 +33,13 @@
 //   reduce    (CE forward): pass A only.
 //
 // Sparse columns (the label, the teacher's top-k ids).  Streaming mode gathers their
-// logits from the staged tiles as they pass and rewrites their gradient after the
-// bulk store of the row and a barrier.  Self-contained mode folds the label into
+// logits from the staged tiles as they pass and rewrites their gradient after every
+// gradient store of the row and a barrier.  Self-contained mode folds the label into
 // pass B and gathers the support logits from global memory before pass A (the row is
-// not written until after it) for the KL loss; after a barrier that follows the row's
-// pass B it adds -coef * p_q at the support columns with reduction adds (fp32), or
-// rewrites those columns with their whole gradient from the gathered logits (bf16,
-// so that every element is rounded once).
+// not written until after it) for the KL loss; once every warp's pass B of the row is
+// done (a barrier, or an mbarrier each warp arrives on after it) it adds -coef * p_q at
+// the support columns with reduction adds (fp32), or rewrites those columns with their
+// whole gradient from the gathered logits (bf16, so that every element is rounded once).
 //
 // Sources: aprender-train wgpu_cross_entropy.rs (module doc, forward_async,
 // backward: loss = lse - s[label], gradient scale * (softmax - onehot), loss
@@ -751,7 +752,7 @@ struct Pending {
     // writes lse, stats and the out-of-window loss), bit 3 the row is split over the cluster;
     // bits 8-9 the cluster exchange buffer of
     // the row's statistics and bit 10 the phase to wait for; bits 16-19 the buffer of the
-    // warps' pass A partials (CE) and bit 20 its phase
+    // warps' pass A partials (CE; KL without a barrier) and bit 20 its phase
     uint32_t f;
     __device__ __forceinline__ bool inwin() const { return f & 1u; }
     __device__ __forceinline__ bool bad() const { return f & 2u; }

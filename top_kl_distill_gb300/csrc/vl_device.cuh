@@ -274,16 +274,6 @@ __device__ __forceinline__ void ms_add(MaxSum& a, float x) {
     a.s += ex2((x - a.m) * kLog2e);
 }
 
-__device__ __forceinline__ void ms_add4(MaxSum& a, float4 v) {
-    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    if (mx > a.m) {
-        a.s = a.s * ex2((a.m - mx) * kLog2e);
-        a.m = mx;
-    }
-    a.s += (ex2((v.x - a.m) * kLog2e) + ex2((v.y - a.m) * kLog2e)) +
-           (ex2((v.z - a.m) * kLog2e) + ex2((v.w - a.m) * kLog2e));
-}
-
 __device__ __forceinline__ float warp_sum(float a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
