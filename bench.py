@@ -428,7 +428,7 @@ class TopK(Case):
 
 class LargeV(Case):
     """CE and top-k KL of 8192 rows x 128256 columns in one pass (vl_ce_kl_fused: each row
-    read once and its combined gradient written once, a row per 4-CTA cluster), and the
+    read once and its combined gradient written once, a row per 3-CTA cluster), and the
     windowed CE mean."""
 
     def __init__(self, torch, w, nbuf):
