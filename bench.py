@@ -1045,7 +1045,7 @@ def main():
     kernel_ms = k_ms_total / args.steps
     e2e_ms, h2d, d2h, e2e_ok = (None, 0, 0, None)
     if isinstance(case, CeFused) and not shard and not args.no_oracle:
-        e2e_ms, h2d, d2h, e2e_ok = e2e_ce(torch, case, max(10, args.steps // 4), 3)
+        e2e_ms, h2d, d2h, e2e_ok = e2e_ce(torch, case, max(30, args.steps), 3)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
